@@ -1,0 +1,19 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """The built C-ABI library (GPU tests only)."""
+    import softmax_l1_norm_gb300 as smla
+    return smla

@@ -1,0 +1,136 @@
+"""Plant plausible mistakes in a private copy of the oracle and check that
+each one fails at least one pin (so the pins would catch the same mistake in
+the real oracle).  Mistakes are planted only in the copy, on the CPU."""
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+
+import oracle_pins as P
+
+ORACLE_FILE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                           "oracle", "smla_oracle.py")
+
+
+def fresh_oracle():
+    spec = importlib.util.spec_from_file_location("smla_oracle_copy", ORACLE_FILE)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _mut_drop_scale(m):
+    orig = m.simple_softmax
+    m.simple_softmax = lambda q, k, v, lse, scale: orig(q, k, v, lse, 1.0)
+
+
+def _mut_sign(m):
+    def f(q, k, v, lse, scale):
+        x = (q @ k.T) * scale
+        p = np.zeros_like(x)
+        p[:, v] = np.exp(np.asarray(lse)[:, None] - x[:, v])
+        return p
+    m.simple_softmax = f
+
+
+def _mut_sum_not_mean(m):
+    m.reduce_sum_g_mean = lambda p: p.sum(axis=0)
+
+
+def _mut_divide_by_slots(m):
+    m.reduce_sum_g_mean = lambda p: p.sum(axis=0) / p.shape[1]
+
+
+def _mut_causal_off_by_one(m):
+    orig = m.slot_valid
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
+        ok = orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=0, topk_len=topk_len)
+        if mask_mode == 3:
+            ok &= j < (r + Sk - Sq)
+        return ok
+    m.slot_valid = f
+
+
+def _mut_causal_top_left(m):
+    orig = m.slot_valid
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
+        ok = orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=0, topk_len=topk_len)
+        if mask_mode == 3:
+            ok &= j <= r
+        return ok
+    m.slot_valid = f
+
+
+def _mut_ignore_topk_length(m):
+    orig = m.slot_valid
+    m.slot_valid = lambda j, *, r, Sq, Sk, mask_mode, topk_len: orig(
+        j, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=None)
+
+
+def _mut_mask_on_slot(m):
+    """causal test applied to the slot number instead of the key position"""
+    orig = m.slot_valid
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
+        ok = orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=0, topk_len=topk_len)
+        if mask_mode == 3:
+            ok &= np.arange(len(j)) <= (r + Sk - Sq)
+        return ok
+    m.slot_valid = f
+
+
+def _mut_lse_head_order(m):
+    orig = m.simple_softmax
+    m.simple_softmax = lambda q, k, v, lse, scale: orig(q, k, v, np.asarray(lse)[::-1], scale)
+
+
+def _mut_tnd_key_offset(m):
+    orig = m.token_geometry
+    def f(*a, **k):
+        return [(b, r, Sq, 0, Sk) for (b, r, Sq, k0, Sk) in orig(*a, **k)]
+    m.token_geometry = f
+
+
+def _mut_keep_out_of_range(m):
+    orig = m.slot_valid
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
+        ok = orig(np.where(j >= Sk, 0, j), r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=topk_len)
+        return ok
+    m.slot_valid = f
+
+
+def _mut_log2(m):
+    def f(q, k, v, lse, scale):
+        x = (q @ k.T) * scale
+        p = np.zeros_like(x)
+        p[:, v] = np.exp2(x[:, v] - np.asarray(lse)[:, None])
+        return p
+    m.simple_softmax = f
+
+
+def _mut_lse_no_scale(m):
+    orig = m.softmax_lse
+    def f(*a, **k):
+        k = dict(k)
+        k["softmax_scale"] = 1.0
+        return orig(*a, **k)
+    m.softmax_lse = f
+
+
+MUTANTS = [_mut_drop_scale, _mut_sign, _mut_sum_not_mean, _mut_divide_by_slots,
+           _mut_causal_off_by_one, _mut_causal_top_left, _mut_ignore_topk_length,
+           _mut_mask_on_slot, _mut_lse_head_order, _mut_tnd_key_offset,
+           _mut_keep_out_of_range, _mut_log2, _mut_lse_no_scale]
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__[5:])
+def test_mutant_is_caught(mutant):
+    m = fresh_oracle()
+    mutant(m)
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(m)
+        except Exception as e:  # AssertionError or a crash both count as caught
+            failed.append((pin.__name__, type(e).__name__))
+    assert failed, f"mutant {mutant.__name__} passed every pin"
