@@ -1,0 +1,469 @@
+#!/usr/bin/env python3
+"""Benchmark: Sparse-Flash-MLA Softmax-L1Norm forward on GB300.
+
+One step = one launch of the fused kernel over the whole workload (gather,
+Q.K^T on the tensor cores, scale/mask/exp against the LSE, head-group mean,
+store).  Default workload: the DeepSeek-V3.2-like sparse causal
+configuration (BSND, B=1, S1=S2=4096, N1=128, D=512, bf16, top-2048 of the
+causally visible keys, right-down causal mask).
+
+Prints ONE JSON line (rank 0).  ``value`` is selected query-key pairs per
+second (a pair = one 512-long per-head dot product on a kept slot), whole job.
+
+  python bench.py [--steps K] [--warmup W] [--config N] [--impl ours|reference]
+  torchrun --nproc-per-node N bench.py --gpus N ...   (independent replicas)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "selected q.k pairs/s (Softmax-L1Norm forward, whole job)"
+UNIT = "pairs/s"
+L2_FLUSH_BYTES = 512 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "smla_fused_kernel_dsv32_traffic.txt")
+KERNEL_SRC = os.path.join(ROOT, "softmax_l1_norm_gb300", "csrc", "smla_kernel.cu")
+
+
+# ----------------------------------------------------------------------------
+def workload_numbers(w):
+    """Pairs, FLOPs and algorithmic bytes of one pass over the workload."""
+    valid = w.valid_slot_count()
+    pairs = valid * w.G
+    flops = 2 * w.head_dim * pairs
+    n = w.n_tokens
+    bytes_ = {
+        "k_gathered": valid * w.head_dim * 2,
+        "q": n * w.G * w.head_dim * 2,
+        "lse": n * w.G * 4,
+        "out": n * w.out_width * 4,
+        "indices": 0 if w.sparse_indices is None else n * w.topk * 4,
+        "topk_length": 0 if w.topk_length is None else n * 4,
+    }
+    return pairs, flops, bytes_
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_sha():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(config_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    kv = {}
+    with open(PROFILE_TRAFFIC) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_sha256_16") != kernel_sha() or kv.get("workload") != config_name:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="smla_clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                n += 1
+                for name, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": float(np.median(load)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ----------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def all_max(x, world, device=None):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+_ORACLE_CHILD = r"""
+import json, sys, time
+import numpy as np
+P = json.loads(sys.argv[1])
+sys.path.insert(0, P["root"])
+import workloads as W, oracle
+w = W.make_config(P["config"])
+kw = dict(dtype=w.dtype, sparse_indices=w.sparse_indices, topk_length=w.topk_length,
+          cu_seqlens_q=w.cu_seqlens_q, cu_seqlens_k=w.cu_seqlens_k, softmax_scale=w.softmax_scale,
+          max_seqlen_k=w.max_seqlen_k, mask_mode=w.mask_mode, layout=w.layout)
+tab = w.token_table()
+def kept(t):
+    b, r, Sq, k0, Sk = (int(x) for x in tab[t])
+    if w.sparse_indices is None:
+        return min(Sk, max(0, r + Sk - Sq + 1)) if w.mask_mode == 3 else Sk
+    idx = w.sparse_indices.reshape(w.n_tokens, -1)[t].astype(np.int64)
+    ok = (idx >= 0) & (idx < Sk)
+    if w.mask_mode == 3:
+        ok &= idx <= r + Sk - Sq
+    if w.topk_length is not None:
+        ok &= np.arange(len(idx)) < int(w.topk_length.reshape(-1)[t])
+    return int(ok.sum())
+rows = np.random.Generator(np.random.PCG64(P["seed"])).permutation(w.n_tokens).tolist()
+pos = 0
+def one(n):
+    global pos
+    pairs = 0
+    t0 = time.perf_counter()
+    for _ in range(n):
+        t = rows[pos % len(rows)]
+        pos += 1
+        oracle.softmax_l1_norm_rows(w.q_bits, w.k_bits, w.softmax_lse, [t], **kw)
+        pairs += kept(t) * w.G
+    return pairs, time.perf_counter() - t0
+res = {"warmup": [], "steps": []}
+per_row = None
+for _ in range(P["warmup"]):
+    p, dt = one(1)
+    per_row = dt if per_row is None else min(per_row, dt)
+    res["warmup"].append([1, p, dt])
+n = max(1, int(P["step_seconds"] / max(per_row or P["step_seconds"], 1e-6)))
+for _ in range(P["steps"]):
+    p, dt = one(n)
+    res["steps"].append([n, p, dt])
+print(json.dumps(res))
+"""
+
+
+def cpu_oracle_run(config, warmup, steps, step_seconds, threads, seed=0):
+    """Time the CPU oracle, as it stands, on bounded samples of the workload's
+    rows: ``warmup`` single rows, then ``steps`` steps of about
+    ``step_seconds`` each.  Runs in a child process so the BLAS thread count
+    is fixed before numpy loads and no CUDA context is involved."""
+    params = json.dumps({"root": ROOT, "config": config, "seed": seed, "warmup": max(1, warmup),
+                         "steps": steps, "step_seconds": step_seconds})
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, "-c", _ORACLE_CHILD, params], capture_output=True, text=True,
+                       env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(f"cpu oracle run failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: each step runs it on a bounded
+    sample of the same workload (rank 0 only; other ranks exit at once)."""
+    if rank != 0:
+        return 0
+    threads = host_threads()
+    r = cpu_oracle_run(args.config, args.warmup, args.steps, args.ref_step_seconds, threads)
+    rows = sum(s[0] for s in r["steps"])
+    pairs = sum(s[1] for s in r["steps"])
+    secs = sum(s[2] for s in r["steps"])
+    name = W.config_names()[args.config]
+    value = pairs / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": name, "note": "CPU fp64 oracle on a bounded random sample of rows per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} random rows of {name} over {args.steps} steps "
+                                   f"(~{args.ref_step_seconds}s each)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import softmax_l1_norm_gb300 as smla
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+
+    w = W.make_config(args.config)
+    name = W.config_names()[args.config]
+    pairs, flops, bytes_ = workload_numbers(w)
+    alg_bytes = sum(bytes_.values())
+
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    host = {
+        "q": torch.from_numpy(w.q_bits.view(np.int16)).view(tdt),
+        "k": torch.from_numpy(w.k_bits.view(np.int16)).view(tdt),
+        "lse": torch.from_numpy(np.ascontiguousarray(w.softmax_lse, dtype=np.float32)),
+        "indices": None if w.sparse_indices is None else torch.from_numpy(w.sparse_indices),
+        "topk_length": None if w.topk_length is None else torch.from_numpy(w.topk_length),
+    }
+    dev = {k: (None if v is None else v.to(device)) for k, v in host.items()}
+    plan = smla.Plan(layout=w.layout, dtype=w.dtype, num_heads_q=w.G, batch_size=w.batch,
+                     max_seqlen_q=w.max_seqlen_q if w.layout == "BSND" else 0,
+                     max_seqlen_k=w.k_bits.shape[1] if w.layout == "BSND" else w.max_seqlen_k,
+                     topk=w.topk, mask_mode=w.mask_mode, softmax_scale=w.softmax_scale,
+                     has_topk_length=w.topk_length is not None,
+                     cu_seqlens_q=None if w.cu_seqlens_q is None else w.cu_seqlens_q.tolist(),
+                     cu_seqlens_k=None if w.cu_seqlens_k is None else w.cu_seqlens_k.tolist())
+    out = torch.empty(plan.output_shape, dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def step():
+        plan.run(dev["q"], dev["k"], dev["lse"], sparse_indices=dev["indices"],
+                 topk_length=dev["topk_length"], out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    code, flags = plan.status(stream)
+    if code != smla.SMLA_OK:
+        raise RuntimeError(f"device status {code} flags {flags} during warm-up")
+    # sanity: every output finite and kept slots non-negative
+    if not bool(torch.isfinite(out).all()):
+        raise RuntimeError("non-finite output")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    gpu_uuid = None
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(device).uuid)
+        if not gpu_uuid.startswith("GPU-"):
+            gpu_uuid = "GPU-" + gpu_uuid
+    except Exception:
+        pass
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    with ClockSampler(gpu_uuid if gpu_uuid else local) as clocks:
+        time.sleep(0.3)
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()          # L2 flush between timed launches (outside the events)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+        wall = time.perf_counter() - wall0
+    barrier(world, device)
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_s = sum(times_ms) / 1000.0
+    max_s = all_max(kernel_s, world, device)
+    clk = clocks.summary()
+    code, flags = plan.status(stream)
+    if code != smla.SMLA_OK:
+        raise RuntimeError(f"device status {code} flags {flags} in the timed region")
+
+    # ------------------------------------------------ end to end through the host API
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: (None if v is None else v.pin_memory()) for k, v in host.items()}
+        pin["out"] = torch.empty(plan.output_shape, dtype=torch.float32).pin_memory()
+        dev2 = dict(dev)
+        dev2["out"] = out
+        e_steps = max(3, min(args.steps, args.e2e_steps))
+        for _ in range(2):
+            plan.run_from_host(pin, dev2, stream=stream)
+        torch.cuda.synchronize(device)
+        barrier(world, device)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(e_steps):
+            plan.run_from_host(pin, dev2, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_s = all_max(ev0.elapsed_time(ev1) / 1000.0, world, device)
+        sizes = plan.io_sizes
+        h2d = sizes.q_bytes + sizes.k_bytes + sizes.lse_bytes + sizes.indices_bytes + sizes.topk_length_bytes
+        e2e = {"value": world * pairs * e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(sizes.out_bytes), "steps": e_steps,
+               "ms_per_step": 1000 * e2e_s / e_steps}
+
+    if rank != 0:
+        return 0
+
+    # ------------------------------------------------ CPU oracle baseline
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        threads = host_threads()
+        r = cpu_oracle_run(args.config, 1, 1, args.cpu_seconds, threads)
+        n_rows, c_pairs, c_secs = r["steps"][0]
+        cpu = {"value": c_pairs / c_secs, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n_rows} random rows of {name} in {c_secs:.1f}s (fp64 numpy, BLAS threads={threads})"}
+
+    hbm_gbs, bf16_tf, src = load_peaks()
+    per_launch_s = kernel_s / args.steps
+    achieved_gbs = alg_bytes / per_launch_s / 1e9
+    achieved_tf = flops / per_launch_s / 1e12
+    traffic = profiled_traffic(name)
+    t_hbm = alg_bytes / (hbm_gbs * 1e9)
+    t_tc = flops / (bf16_tf * 1e12)
+    line = {
+        "metric": METRIC, "value": world * pairs * args.steps / max_s, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * max_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded numpy; q,k ~ N(0,1); LSE = expected value, see DESIGN)",
+        "config": {"workload": name, "layout": w.layout, "B": w.batch, "S1": w.max_seqlen_q,
+                   "S2": int(w.k_bits.shape[1]) if w.layout == "BSND" else None, "N1": w.G, "D": w.head_dim,
+                   "topk": w.topk, "mask_mode": w.mask_mode, "pairs_per_step": pairs,
+                   "flops_per_step": flops, "algorithmic_bytes_per_step": alg_bytes,
+                   "parallelism": f"replicas x{world}", "l2": "flushed (512 MB write) before every timed launch"},
+        "tflops": world * flops * args.steps / max_s / 1e12,
+        "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+                     "achieved": achieved_gbs if t_hbm >= t_tc else achieved_tf,
+                     "peak": hbm_gbs if t_hbm >= t_tc else bf16_tf,
+                     "unit": "GB/s" if t_hbm >= t_tc else "TFLOP/s",
+                     "frac": (achieved_gbs / hbm_gbs) if t_hbm >= t_tc else (achieved_tf / bf16_tf),
+                     "traffic": traffic, "peak_source": src,
+                     "roofline_ms": 1000 * max(t_hbm, t_tc), "kernel_ms": 1000 * per_launch_s},
+        "roofline_tensor": {"achieved": achieved_tf, "peak": bf16_tf, "unit": "TFLOP/s",
+                            "frac": achieved_tf / bf16_tf, "peak_source": src},
+        "clocks": clk,
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "wall_s_timed_region": wall,
+        "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "stages", "mma_n",
+                                                                        "smem_bytes", "max_cta_cost",
+                                                                        "mean_cta_cost")},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,252 @@
+/*
+ * smla_l1norm.h -- C ABI of the GB300 Sparse-Flash-MLA Softmax-L1Norm forward.
+ *
+ * The operator (article "SparseFlashMlaSoftmaxL1Norm", CANN ops-transformer,
+ * section 三阶段计算公式 / three-stage formula):
+ *
+ *   stage 1  selectedKv = Gather(K, sparse_indices[row, i]), 0 <= i < topk
+ *            (or the whole K when there are no sparse indices);
+ *   stage 2  P[g, i] = exp(scale * q[row, g] . selectedKv[i] - softmax_lse[row, g])
+ *            for every slot that the mask keeps, 0 for the others;
+ *   stage 3  out[row, i] = (sum over g < G of P[g, i]) / G,   G = N1 / N2.
+ *
+ * A slot is kept when its key position j lies inside the row's sequence
+ * (0 <= j < Sk), its slot number is below topk_length[row] (when given), and,
+ * for mask_mode 3 (rightDownCausal, the lower triangle divided at the
+ * right-bottom vertex), j <= r + Sk - Sq for local query row r.  Kept slots
+ * never depend on other slots; every output element is written exactly once
+ * (no atomics), so results are bitwise reproducible run to run (the article's
+ * constraints section states the operator is deterministic).
+ *
+ * Call pattern (the article's two-phase design: a metadata operator that
+ * balances rows over cores, then the main operator):
+ *
+ *   smla_l1norm_plan_create()   once per shape: validate, build the CTA work
+ *                               schedule on the host, upload it (the GB300
+ *                               counterpart of SparseFlashMlaSoftmaxL1NormMetadata)
+ *   smla_l1norm_run()           per call: one kernel launch on the caller's
+ *                               stream; asynchronous; allocates nothing
+ *   smla_l1norm_get_status()    optional: device-side warnings / timeouts
+ *   smla_l1norm_plan_destroy()
+ *
+ * Memory ownership: the caller owns every tensor.  All tensors are dense and
+ * row-major ("AutoContiguous" in the article's operator definition) with the
+ * shapes below; device pointers must be 16-byte aligned.  A plan owns one
+ * small device buffer (its work list and status word).  A plan is bound to the
+ * device that was current when it was created; two run() calls with the same
+ * plan may overlap on the GPU, but they then share the status word.
+ *
+ * Error codes follow the article's aclnn split between null pointers
+ * (ACLNN_ERR_PARAM_NULLPTR) and invalid parameters (ACLNN_ERR_PARAM_INVALID):
+ * host-side checks return before any CUDA call or launch.
+ */
+#ifndef SMLA_L1NORM_H_
+#define SMLA_L1NORM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *smla_stream_t;
+
+typedef enum {
+  SMLA_OK = 0,
+  SMLA_ERR_NULLPTR = 1,      /* a required pointer is NULL                         */
+  SMLA_ERR_INVALID = 2,      /* a shape / layout / dtype / constraint is violated  */
+  SMLA_ERR_UNSUPPORTED = 3,  /* a documented feature this library does not build:
+                                cmp_ratio != 1, mask modes other than 0 and 3     */
+  SMLA_ERR_CUDA = 4,         /* a CUDA runtime call failed (see get_last_cuda_error) */
+  SMLA_ERR_TIMEOUT = 5,      /* a device-side wait gave up (reported by get_status) */
+  SMLA_WARN_BAD_INDEX = 6    /* a sparse index outside [-1, Sk) was seen and treated
+                                as masked (reported by get_status)                 */
+} smla_status;
+
+typedef enum { SMLA_LAYOUT_BSND = 0, SMLA_LAYOUT_TND = 1 } smla_layout;
+typedef enum { SMLA_DTYPE_F16 = 0, SMLA_DTYPE_BF16 = 1 } smla_dtype;
+typedef enum { SMLA_MASK_NONE = 0, SMLA_MASK_RIGHT_DOWN_CAUSAL = 3 } smla_mask_mode;
+
+/*
+ * Operator description (article: parameter tables 参数说明 for the main
+ * operator and the metadata operator; constraints 约束说明).
+ *
+ *   layout_q, layout_k  BSND or TND; must be equal.
+ *   dtype               q and k share it (FLOAT16 or BFLOAT16).
+ *   num_heads_q         N1, 1..128.   num_heads_k  N2, must be 1.   G = N1 / N2.
+ *   head_dim            D, must be 512.
+ *   batch_size          BSND: B (>= 0).  TND: the number of sequences (the
+ *                       cu_seqlens arrays hold batch_size + 1 entries).
+ *   max_seqlen_q        BSND: S1 (>= 0).  TND: ignored.
+ *   max_seqlen_k        BSND: S2 (>= 0).  TND: output width of the dense form
+ *                       (must be >= every sequence's key length; ignored when
+ *                       topk > 0).
+ *   topk                last dimension of sparse_indices; 0 = dense form.
+ *   mask_mode           0 (none) or 3 (rightDownCausal).
+ *   cmp_ratio           key compression ratio; only 1 is built.
+ *   softmax_scale       multiplies q.k before the exp (the article's default
+ *                       is 1.0 and it recommends 1/sqrt(head_dim)).
+ *   has_topk_length     1 if run() will be given topk_length.
+ *   cu_seqlens_q/k      TND only: HOST arrays of batch+1 int32, cumulative
+ *                       sums of the per-sequence query / key lengths,
+ *                       starting at 0 and non-decreasing.  Read during
+ *                       plan_create only.
+ *   topk_length_hint    optional HOST array (one int32 per query token): the
+ *                       expected topk_length, used only to balance the work
+ *                       schedule.  NULL = estimate min(topk, visible keys).
+ *   num_ctas            0 = one persistent CTA per SM of the current device;
+ *                       > 0 forces a grid size (tests, multi-tenant use).
+ */
+typedef struct {
+  int32_t layout_q;
+  int32_t layout_k;
+  int32_t dtype;
+  int32_t num_heads_q;
+  int32_t num_heads_k;
+  int32_t head_dim;
+  int32_t batch_size;
+  int32_t max_seqlen_q;
+  int32_t max_seqlen_k;
+  int32_t topk;
+  int32_t mask_mode;
+  int32_t cmp_ratio;
+  float softmax_scale;
+  int32_t has_topk_length;
+  const int32_t *cu_seqlens_q;
+  const int32_t *cu_seqlens_k;
+  const int32_t *topk_length_hint;
+  int32_t num_ctas;
+} smla_l1norm_desc;
+
+typedef struct smla_plan smla_plan; /* opaque */
+
+/* Summary of a plan's schedule (costs in the scheduler's tile units). */
+typedef struct {
+  int64_t num_tokens;      /* query tokens (B*S1 or T1)                          */
+  int64_t num_items;       /* work items (a token, or a pack of tokens if dense) */
+  int32_t num_ctas;        /* persistent grid size                               */
+  int32_t rows_per_item;   /* R: query tokens packed into one MMA (dense form)   */
+  int32_t mma_n;           /* N of the tensor-core instruction (R*G padded to 16) */
+  int32_t stages;          /* depth of the shared-memory key ring                */
+  int32_t smem_bytes;      /* dynamic shared memory per CTA                      */
+  int32_t out_width;       /* last output dimension                              */
+  int64_t est_tiles;       /* 128-key tiles the schedule expects                 */
+  double max_cta_cost;     /* heaviest CTA                                       */
+  double mean_cta_cost;    /* average CTA                                        */
+  int64_t q_rows_total;    /* rows of the 2-D view of q (tokens * G)             */
+  int64_t k_rows_total;    /* rows of the 2-D view of k (B*S2 or T2)             */
+} smla_plan_info;
+
+/*
+ * Validate ``desc`` and build a plan for the current CUDA device.
+ * Returns SMLA_ERR_NULLPTR / SMLA_ERR_INVALID / SMLA_ERR_UNSUPPORTED without
+ * touching the GPU when the description is rejected; SMLA_ERR_CUDA if the
+ * device query, allocation or upload fails.  An empty q (no query token)
+ * gives a valid plan whose run() returns at once, as the article's
+ * constraints section specifies for an empty q tensor.
+ * Synchronous (the work list is uploaded with a blocking copy).
+ */
+smla_status smla_l1norm_plan_create(const smla_l1norm_desc *desc, smla_plan **plan_out);
+
+/* Free a plan and its device buffer.  NULL is ignored.  The caller must make
+ * sure no run() using the plan is still executing. */
+void smla_l1norm_plan_destroy(smla_plan *plan);
+
+/* Output shape (infershape in the article): BSND -> 4 dims (B, S1, 1, W),
+ * TND -> 3 dims (T1, 1, W); W = topk when sparse, else S2 (BSND) or
+ * max_seqlen_k (TND). */
+smla_status smla_l1norm_output_shape(const smla_plan *plan, int64_t dims[4], int32_t *ndim);
+
+smla_status smla_l1norm_plan_get_info(const smla_plan *plan, smla_plan_info *info);
+
+/*
+ * Compute the operator on ``stream`` (asynchronous; one kernel launch; no
+ * allocation, no host synchronisation).  Device pointers, 16-byte aligned:
+ *
+ *   q               (B,S1,N1,512) or (T1,N1,512)  fp16/bf16  [required]
+ *   k               (B,S2,1,512)  or (T2,1,512)   same dtype [required unless
+ *                   there is no key row at all]
+ *   softmax_lse     (B,1,S1,G)    or (1,T1,G)     fp32       [required]
+ *   sparse_indices  (B,S1,1,topk) or (T1,1,topk)  int32      [required iff topk > 0]
+ *                   key positions inside the row's sequence; -1 is padding
+ *   topk_length     (B,S1,1)      or (T1,1)       int32      [required iff the
+ *                   plan says has_topk_length]; values are clamped to [0, topk]
+ *   out             output_shape()                fp32       [required]
+ *
+ * Every element of ``out`` is written (masked and padding slots as 0.0f), so
+ * it need not be cleared.  Returns SMLA_ERR_NULLPTR for a missing required
+ * pointer, SMLA_ERR_INVALID for a misaligned one, SMLA_ERR_CUDA if the
+ * launch fails.  Device-side conditions (index out of range, wait timeout)
+ * are recorded in the plan's status word; see smla_l1norm_get_status().
+ */
+smla_status smla_l1norm_run(const smla_plan *plan, const void *q, const void *k,
+                            const float *softmax_lse, const int32_t *sparse_indices,
+                            const int32_t *topk_length, float *out, smla_stream_t stream);
+
+/* Host-side sizes, in bytes, of the tensors run() reads and writes. */
+typedef struct {
+  size_t q_bytes, k_bytes, lse_bytes, indices_bytes, topk_length_bytes, out_bytes;
+} smla_io_sizes;
+
+smla_status smla_l1norm_io_sizes(const smla_plan *plan, smla_io_sizes *sizes);
+
+/*
+ * End-to-end form for callers whose tensors live in HOST memory: on
+ * ``stream``, copy each host input into the caller's device buffer of the
+ * same role (cudaMemcpyAsync, one copy per tensor), run, and copy the output
+ * back to ``h_out``.  Host buffers should be page-locked for the copies to be
+ * asynchronous.  Pass NULL for tensors the plan does not use.  Returns as
+ * run(); the host output is valid after the stream is synchronised.
+ */
+smla_status smla_l1norm_run_from_host(const smla_plan *plan,
+                                      const void *h_q, const void *h_k, const float *h_lse,
+                                      const int32_t *h_indices, const int32_t *h_topk_length,
+                                      float *h_out,
+                                      void *d_q, void *d_k, float *d_lse, int32_t *d_indices,
+                                      int32_t *d_topk_length, float *d_out,
+                                      smla_stream_t stream);
+
+/*
+ * Read and clear the plan's device status word.  Synchronises ``stream``.
+ * Writes the raw flag bits to *flags (if non-NULL): bit 0 = bad index seen,
+ * bit 1 = a device-side wait timed out.  Returns SMLA_ERR_TIMEOUT if bit 1 is
+ * set, else SMLA_WARN_BAD_INDEX if bit 0 is set, else SMLA_OK.
+ */
+smla_status smla_l1norm_get_status(const smla_plan *plan, smla_stream_t stream, int32_t *flags);
+
+/*
+ * Host-only view of the scheduler, for inspection and tests: validate
+ * ``desc`` and build the schedule for ``num_ctas`` CTAs without any CUDA
+ * call.  If ``items`` is non-NULL it receives up to ``items_capacity`` work
+ * items of 8 int32 each, grouped by CTA (fields: first token, tokens in the
+ * item, local row of the first token, first key row of the sequence, Sq, Sk,
+ * key tiles of a dense item, reserved); ``cta_offsets`` (num_ctas + 1 int32)
+ * receives where each CTA's items start.  ``info`` receives the summary.
+ */
+smla_status smla_l1norm_schedule_host(const smla_l1norm_desc *desc, int32_t num_ctas,
+                                      int32_t *items, int64_t items_capacity,
+                                      int32_t *cta_offsets, smla_plan_info *info);
+
+/*
+ * Self-test of the device-side wait bound (the article has no counterpart):
+ * launches one CTA whose only thread waits, with the bounded wait every
+ * role of the fused kernel uses, on a barrier that nothing completes.  After
+ * ``timeout_ns`` the wait gives up and records the timeout flag; the call
+ * synchronises ``stream`` and returns SMLA_ERR_TIMEOUT (flags bit 1) when the
+ * bound works.  Allocates and frees 4 bytes of device memory.
+ */
+smla_status smla_debug_wait_timeout_probe(int64_t timeout_ns, smla_stream_t stream, int32_t *flags);
+
+/* Static description of a status code. */
+const char *smla_status_string(smla_status status);
+
+/* Text of the last CUDA error seen by this library on this thread ("" if none). */
+const char *smla_get_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMLA_L1NORM_H_ */

@@ -1,0 +1,600 @@
+// Host side of the C ABI declared in include/smla_l1norm.h: validation,
+// the CTA work schedule (the GB300 counterpart of the article's metadata
+// operator), tensor-map encoding and the launch.
+//
+// Validation follows the article "SparseFlashMlaSoftmaxL1Norm" (CANN
+// ops-transformer): parameter tables (参数说明), constraints (约束说明) and the
+// aclnn error split between null pointers and invalid parameters.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <numeric>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "../../include/smla_l1norm.h"
+#include "smla_internal.h"
+
+namespace smla {
+cudaError_t launch_wait_timeout_probe(int32_t* status, int64_t timeout_ns, cudaStream_t stream);
+}
+
+using smla::WorkItem;
+
+namespace {
+
+thread_local std::string g_last_cuda_error;
+
+smla_status cuda_fail(cudaError_t e, const char* what) {
+  g_last_cuda_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return SMLA_ERR_CUDA;
+}
+
+constexpr int kDefaultSmemOptin = 232448;  // 227 KB, the sm_100-family opt-in limit
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Geometry {
+  bool sparse = false;
+  bool tnd = false;
+  int G = 0;
+  int R = 1;
+  int n_mma = 16;
+  int width = 0;
+  int64_t n_tokens = 0;
+  int64_t q_rows = 0;
+  int64_t k_rows = 0;
+  int batch = 0;
+  std::vector<int64_t> q0, sq, k0, sk;  // per sequence
+};
+
+// Checks every field of the description; fills the geometry on success.
+smla_status validate(const smla_l1norm_desc* d, Geometry* g) {
+  if (d == nullptr) return SMLA_ERR_NULLPTR;
+  if (d->layout_q != SMLA_LAYOUT_BSND && d->layout_q != SMLA_LAYOUT_TND) return SMLA_ERR_INVALID;
+  if (d->layout_k != d->layout_q) return SMLA_ERR_INVALID;  // layout_q must equal layout_k
+  if (d->dtype != SMLA_DTYPE_F16 && d->dtype != SMLA_DTYPE_BF16) return SMLA_ERR_INVALID;
+  if (d->num_heads_k != 1) return SMLA_ERR_INVALID;                          // N2 only 1
+  if (d->num_heads_q < 1 || d->num_heads_q > 128) return SMLA_ERR_INVALID;   // N1 in 1..128
+  if (d->num_heads_q % d->num_heads_k != 0) return SMLA_ERR_INVALID;
+  if (d->head_dim != smla::kHeadDim) return SMLA_ERR_INVALID;                 // D only 512
+  if (d->mask_mode == 1 || d->mask_mode == 2) return SMLA_ERR_UNSUPPORTED;
+  if (d->mask_mode != 0 && d->mask_mode != 3) return SMLA_ERR_INVALID;
+  if (d->cmp_ratio < 1 || d->cmp_ratio > 128) return SMLA_ERR_INVALID;       // range 1..128
+  if (d->cmp_ratio != 1) return SMLA_ERR_UNSUPPORTED;
+  if (d->topk < 0) return SMLA_ERR_INVALID;
+  if (!std::isfinite(d->softmax_scale)) return SMLA_ERR_INVALID;
+  if (d->has_topk_length != 0 && d->has_topk_length != 1) return SMLA_ERR_INVALID;
+  if (d->has_topk_length && d->topk == 0) return SMLA_ERR_INVALID;  // topk_length needs indices
+  if (d->num_ctas < 0) return SMLA_ERR_INVALID;
+
+  g->sparse = d->topk > 0;
+  g->tnd = d->layout_q == SMLA_LAYOUT_TND;
+  g->G = d->num_heads_q / d->num_heads_k;
+  if (g->tnd) {
+    if (d->cu_seqlens_q == nullptr || d->cu_seqlens_k == nullptr) return SMLA_ERR_NULLPTR;
+    if (d->batch_size < 0) return SMLA_ERR_INVALID;
+    g->batch = d->batch_size;
+    const int32_t* cq = d->cu_seqlens_q;
+    const int32_t* ck = d->cu_seqlens_k;
+    if (cq[0] != 0 || ck[0] != 0) return SMLA_ERR_INVALID;
+    int64_t max_sk = 0;
+    for (int b = 0; b < g->batch; ++b) {
+      if (cq[b + 1] < cq[b] || ck[b + 1] < ck[b]) return SMLA_ERR_INVALID;
+      g->q0.push_back(cq[b]);
+      g->sq.push_back(cq[b + 1] - cq[b]);
+      g->k0.push_back(ck[b]);
+      g->sk.push_back(ck[b + 1] - ck[b]);
+      max_sk = std::max<int64_t>(max_sk, ck[b + 1] - ck[b]);
+    }
+    g->n_tokens = cq[g->batch];
+    g->k_rows = ck[g->batch];
+    if (g->sparse) {
+      g->width = d->topk;
+    } else {
+      if (d->max_seqlen_k < max_sk) return SMLA_ERR_INVALID;  // output width must hold every row
+      g->width = d->max_seqlen_k;
+    }
+  } else {
+    if (d->batch_size < 0 || d->max_seqlen_q < 0 || d->max_seqlen_k < 0) return SMLA_ERR_INVALID;
+    g->batch = d->batch_size;
+    const int64_t S1 = d->max_seqlen_q, S2 = d->max_seqlen_k;
+    for (int b = 0; b < g->batch; ++b) {
+      g->q0.push_back(b * S1);
+      g->sq.push_back(S1);
+      g->k0.push_back(b * S2);
+      g->sk.push_back(S2);
+    }
+    g->n_tokens = static_cast<int64_t>(g->batch) * S1;
+    g->k_rows = static_cast<int64_t>(g->batch) * S2;
+    g->width = g->sparse ? d->topk : static_cast<int>(S2);
+  }
+  if (g->sparse) {
+    g->R = 1;
+  } else {
+    g->R = std::max(1, 128 / g->G);
+  }
+  g->n_mma = static_cast<int>(std::max<int64_t>(16, ceil_div(static_cast<int64_t>(g->R) * g->G, 16) * 16));
+  g->q_rows = g->n_tokens * g->G;
+  // TMA coordinates are 32-bit; keep every row index representable.
+  if (g->q_rows + 256 >= (int64_t{1} << 31) || g->k_rows + 256 >= (int64_t{1} << 31)) return SMLA_ERR_INVALID;
+  if (g->n_tokens * static_cast<int64_t>(g->width) >= (int64_t{1} << 40)) return SMLA_ERR_INVALID;
+  if (d->topk_length_hint != nullptr && !g->sparse) return SMLA_ERR_INVALID;
+  return SMLA_OK;
+}
+
+int visible_keys(int64_t r, int64_t Sq, int64_t Sk, int mask_mode) {
+  if (mask_mode == 0) return static_cast<int>(Sk);
+  return static_cast<int>(std::min<int64_t>(Sk, std::max<int64_t>(0, r + Sk - Sq + 1)));
+}
+
+struct Schedule {
+  std::vector<WorkItem> items;       // grouped by CTA
+  std::vector<int32_t> cta_begin;    // num_ctas + 1
+  int64_t est_tiles = 0;
+  double max_cost = 0, mean_cost = 0;
+};
+
+// Build the work items and deal them to CTAs by longest-processing-time
+// first: items sorted by estimated cost, each given to the least-loaded CTA.
+// Any assignment gives the same output bits; the schedule only balances
+// time.  Cost of an item: its 128-key tiles, plus a per-token overhead for
+// the q load and the zero tail.
+Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ctas) {
+  Schedule s;
+  std::vector<WorkItem> items;
+  std::vector<double> cost;
+  const double row_overhead = 0.05 + 0.35 * (g.n_mma / 128.0);
+  for (int b = 0; b < g.batch; ++b) {
+    const int64_t Sq = g.sq[b], Sk = g.sk[b];
+    if (g.sparse) {
+      for (int64_t r = 0; r < Sq; ++r) {
+        const int64_t tok = g.q0[b] + r;
+        int64_t n;
+        if (d->topk_length_hint != nullptr) {
+          n = std::min<int64_t>(std::max<int32_t>(d->topk_length_hint[tok], 0), d->topk);
+        } else if (d->has_topk_length) {
+          n = std::min<int64_t>(d->topk, visible_keys(r, Sq, Sk, d->mask_mode));
+        } else {
+          n = d->topk;
+        }
+        if (Sk == 0) n = 0;
+        const int64_t tiles = ceil_div(n, smla::kTileKeys);
+        WorkItem w{static_cast<int32_t>(tok), 1, static_cast<int32_t>(r), static_cast<int32_t>(g.k0[b]),
+                   static_cast<int32_t>(Sq), static_cast<int32_t>(Sk), 0, 0};
+        items.push_back(w);
+        cost.push_back(static_cast<double>(tiles) + row_overhead +
+                       0.02 * static_cast<double>(g.width - tiles * smla::kTileKeys) / smla::kTileKeys);
+        s.est_tiles += tiles;
+      }
+    } else {
+      for (int64_t r0 = 0; r0 < Sq; r0 += g.R) {
+        const int64_t nrows = std::min<int64_t>(g.R, Sq - r0);
+        const int64_t vis = visible_keys(r0 + nrows - 1, Sq, Sk, d->mask_mode);
+        const int64_t tiles = ceil_div(std::min<int64_t>(vis, g.width), smla::kTileKeys);
+        WorkItem w{static_cast<int32_t>(g.q0[b] + r0), static_cast<int32_t>(nrows), static_cast<int32_t>(r0),
+                   static_cast<int32_t>(g.k0[b]), static_cast<int32_t>(Sq), static_cast<int32_t>(Sk),
+                   static_cast<int32_t>(tiles), 0};
+        items.push_back(w);
+        cost.push_back(static_cast<double>(tiles) + row_overhead +
+                       0.02 * nrows * static_cast<double>(g.width - tiles * smla::kTileKeys) / smla::kTileKeys);
+        s.est_tiles += tiles;
+      }
+    }
+  }
+  const int64_t n = static_cast<int64_t>(items.size());
+  std::vector<int64_t> order(n);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) { return cost[a] > cost[b]; });
+  using Load = std::pair<double, int>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int c = 0; c < num_ctas; ++c) heap.push({0.0, c});
+  std::vector<std::vector<int64_t>> per(num_ctas);
+  std::vector<double> load(num_ctas, 0.0);
+  for (int64_t i : order) {
+    Load l = heap.top();
+    heap.pop();
+    per[l.second].push_back(i);
+    l.first += cost[i];
+    load[l.second] = l.first;
+    heap.push(l);
+  }
+  s.cta_begin.resize(num_ctas + 1);
+  s.items.reserve(n);
+  for (int c = 0; c < num_ctas; ++c) {
+    s.cta_begin[c] = static_cast<int32_t>(s.items.size());
+    // within a CTA, keep token order (neighbouring tokens share keys in L2)
+    std::sort(per[c].begin(), per[c].end());
+    for (int64_t i : per[c]) s.items.push_back(items[i]);
+  }
+  s.cta_begin[num_ctas] = static_cast<int32_t>(s.items.size());
+  if (num_ctas > 0) {
+    s.max_cost = *std::max_element(load.begin(), load.end());
+    s.mean_cost = std::accumulate(load.begin(), load.end(), 0.0) / num_ctas;
+  }
+  return s;
+}
+
+int stages_for(int n_mma, int smem_limit) {
+  int st = smla::kMaxStages;
+  while (st > 2 && smla::smem_bytes_for(n_mma, st) > smem_limit) --st;
+  return st;
+}
+
+uint32_t make_idesc(int dtype, int n_mma) {
+  // tcgen05 instruction descriptor, kind::f16: fp32 accumulator, A and B of
+  // the same 16-bit type, both K-major, M = 128, N = n_mma.
+  const uint32_t ab = dtype == SMLA_DTYPE_BF16 ? 1u : 0u;
+  uint32_t d = 0;
+  d |= 1u << 4;                                    // D format: f32
+  d |= ab << 7;                                    // A format
+  d |= ab << 10;                                   // B format
+  d |= static_cast<uint32_t>(n_mma >> 3) << 17;    // N / 8
+  d |= static_cast<uint32_t>(128 >> 4) << 24;      // M / 16
+  return d;
+}
+
+void fill_info(const Geometry& g, const Schedule& s, int num_ctas, int stages, int smem, smla_plan_info* info) {
+  std::memset(info, 0, sizeof(*info));
+  info->num_tokens = g.n_tokens;
+  info->num_items = static_cast<int64_t>(s.items.size());
+  info->num_ctas = num_ctas;
+  info->rows_per_item = g.R;
+  info->mma_n = g.n_mma;
+  info->stages = stages;
+  info->smem_bytes = smem;
+  info->out_width = g.width;
+  info->est_tiles = s.est_tiles;
+  info->max_cta_cost = s.max_cost;
+  info->mean_cta_cost = s.mean_cost;
+  info->q_rows_total = g.q_rows;
+  info->k_rows_total = g.k_rows;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D view (rows x 512) of a half-precision tensor, boxes of 64 columns x
+// box_rows rows, 128-byte swizzle (the layout the MMA descriptors expect).
+bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int box_rows, int dtype) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(smla::kHeadDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(smla::kHeadDim) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(smla::kChunkElems), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      dtype == SMLA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int64_t wait_timeout_ns() {
+  const char* e = std::getenv("SMLA_WAIT_TIMEOUT_MS");
+  if (e != nullptr) {
+    const long long ms = std::atoll(e);
+    if (ms > 0) return ms * 1000000LL;
+  }
+  return 2000LL * 1000000LL;  // 2 s
+}
+
+}  // namespace
+
+struct smla_plan {
+  smla_l1norm_desc desc;
+  Geometry geo;
+  int device = 0;
+  int num_ctas = 0;
+  int stages = 0;
+  int smem = 0;
+  uint32_t idesc = 0;
+  void* dbuf = nullptr;
+  int32_t* d_status = nullptr;
+  int32_t* d_cta_begin = nullptr;
+  WorkItem* d_items = nullptr;
+  smla_plan_info info{};
+  int64_t timeout_ns = 0;
+};
+
+extern "C" {
+
+smla_status smla_l1norm_schedule_host(const smla_l1norm_desc* desc, int32_t num_ctas, int32_t* items,
+                                      int64_t items_capacity, int32_t* cta_offsets, smla_plan_info* info) {
+  Geometry g;
+  smla_status st = validate(desc, &g);
+  if (st != SMLA_OK) return st;
+  if (num_ctas <= 0) return SMLA_ERR_INVALID;
+  const Schedule s = build_schedule(desc, g, num_ctas);
+  if (items != nullptr) {
+    const int64_t n = std::min<int64_t>(items_capacity, static_cast<int64_t>(s.items.size()));
+    std::memcpy(items, s.items.data(), static_cast<size_t>(n) * sizeof(WorkItem));
+  }
+  if (cta_offsets != nullptr) std::memcpy(cta_offsets, s.cta_begin.data(), s.cta_begin.size() * sizeof(int32_t));
+  if (info != nullptr) {
+    const int stages = stages_for(g.n_mma, kDefaultSmemOptin);
+    fill_info(g, s, num_ctas, stages, smla::smem_bytes_for(g.n_mma, stages), info);
+  }
+  return SMLA_OK;
+}
+
+smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** plan_out) {
+  if (plan_out == nullptr) return SMLA_ERR_NULLPTR;
+  *plan_out = nullptr;
+  Geometry g;
+  smla_status st = validate(desc, &g);
+  if (st != SMLA_OK) return st;
+
+  auto* plan = new smla_plan();
+  plan->desc = *desc;
+  plan->desc.cu_seqlens_q = nullptr;  // host arrays are only read here
+  plan->desc.cu_seqlens_k = nullptr;
+  plan->desc.topk_length_hint = nullptr;
+  plan->geo = g;
+  plan->idesc = make_idesc(desc->dtype, g.n_mma);
+  plan->timeout_ns = wait_timeout_ns();
+
+  cudaError_t e = cudaGetDevice(&plan->device);
+  if (e != cudaSuccess) {
+    delete plan;
+    return cuda_fail(e, "cudaGetDevice");
+  }
+  int sms = 0, optin = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, plan->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, plan->device);
+  if (e != cudaSuccess) {
+    delete plan;
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  }
+  int ctas = desc->num_ctas > 0 ? desc->num_ctas : sms;
+  ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ctas, std::max<int64_t>(1, g.n_tokens))));
+  plan->num_ctas = ctas;
+  plan->stages = stages_for(g.n_mma, optin);
+  plan->smem = smla::smem_bytes_for(g.n_mma, plan->stages);
+  if (plan->smem > optin) {
+    delete plan;
+    return SMLA_ERR_INVALID;
+  }
+  const Schedule s = build_schedule(desc, g, ctas);
+  fill_info(g, s, ctas, plan->stages, plan->smem, &plan->info);
+
+  // one device buffer: status word | CTA offsets | work items
+  const size_t off_begin = 256;
+  const size_t off_items = off_begin + ((s.cta_begin.size() * sizeof(int32_t) + 255) / 256) * 256;
+  const size_t bytes = off_items + std::max<size_t>(1, s.items.size()) * sizeof(WorkItem);
+  e = cudaMalloc(&plan->dbuf, bytes);
+  if (e != cudaSuccess) {
+    delete plan;
+    return cuda_fail(e, "cudaMalloc(plan)");
+  }
+  std::vector<uint8_t> host(bytes, 0);
+  std::memcpy(host.data() + off_begin, s.cta_begin.data(), s.cta_begin.size() * sizeof(int32_t));
+  if (!s.items.empty()) std::memcpy(host.data() + off_items, s.items.data(), s.items.size() * sizeof(WorkItem));
+  e = cudaMemcpy(plan->dbuf, host.data(), bytes, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = smla::configure_fused(plan->smem);
+  if (e != cudaSuccess) {
+    cudaFree(plan->dbuf);
+    delete plan;
+    return cuda_fail(e, "plan upload");
+  }
+  auto* b = static_cast<uint8_t*>(plan->dbuf);
+  plan->d_status = reinterpret_cast<int32_t*>(b);
+  plan->d_cta_begin = reinterpret_cast<int32_t*>(b + off_begin);
+  plan->d_items = reinterpret_cast<WorkItem*>(b + off_items);
+  if (std::getenv("SMLA_LOG") != nullptr) {
+    std::fprintf(stderr,
+                 "[smla] plan: tokens=%lld items=%lld ctas=%d R=%d N=%d stages=%d smem=%d tiles=%lld "
+                 "max/mean cost=%.2f/%.2f\n",
+                 static_cast<long long>(g.n_tokens), static_cast<long long>(s.items.size()), ctas, g.R,
+                 g.n_mma, plan->stages, plan->smem, static_cast<long long>(s.est_tiles), s.max_cost,
+                 s.mean_cost);
+  }
+  *plan_out = plan;
+  return SMLA_OK;
+}
+
+void smla_l1norm_plan_destroy(smla_plan* plan) {
+  if (plan == nullptr) return;
+  if (plan->dbuf != nullptr) cudaFree(plan->dbuf);
+  delete plan;
+}
+
+smla_status smla_l1norm_output_shape(const smla_plan* plan, int64_t dims[4], int32_t* ndim) {
+  if (plan == nullptr || dims == nullptr || ndim == nullptr) return SMLA_ERR_NULLPTR;
+  const Geometry& g = plan->geo;
+  if (g.tnd) {
+    dims[0] = g.n_tokens;
+    dims[1] = 1;
+    dims[2] = g.width;
+    dims[3] = 0;
+    *ndim = 3;
+  } else {
+    dims[0] = g.batch;
+    dims[1] = plan->desc.max_seqlen_q;
+    dims[2] = 1;
+    dims[3] = g.width;
+    *ndim = 4;
+  }
+  return SMLA_OK;
+}
+
+smla_status smla_l1norm_plan_get_info(const smla_plan* plan, smla_plan_info* info) {
+  if (plan == nullptr || info == nullptr) return SMLA_ERR_NULLPTR;
+  *info = plan->info;
+  return SMLA_OK;
+}
+
+smla_status smla_l1norm_io_sizes(const smla_plan* plan, smla_io_sizes* s) {
+  if (plan == nullptr || s == nullptr) return SMLA_ERR_NULLPTR;
+  const Geometry& g = plan->geo;
+  s->q_bytes = static_cast<size_t>(g.q_rows) * smla::kHeadDim * 2;
+  s->k_bytes = static_cast<size_t>(g.k_rows) * smla::kHeadDim * 2;
+  s->lse_bytes = static_cast<size_t>(g.n_tokens) * g.G * 4;
+  s->indices_bytes = g.sparse ? static_cast<size_t>(g.n_tokens) * plan->desc.topk * 4 : 0;
+  s->topk_length_bytes = plan->desc.has_topk_length ? static_cast<size_t>(g.n_tokens) * 4 : 0;
+  s->out_bytes = static_cast<size_t>(g.n_tokens) * g.width * 4;
+  return SMLA_OK;
+}
+
+smla_status smla_l1norm_run(const smla_plan* plan, const void* q, const void* k, const float* softmax_lse,
+                            const int32_t* sparse_indices, const int32_t* topk_length, float* out,
+                            smla_stream_t stream) {
+  if (plan == nullptr) return SMLA_ERR_NULLPTR;
+  const Geometry& g = plan->geo;
+  if (g.n_tokens == 0 || g.width == 0) return SMLA_OK;  // empty q (or empty output): nothing to do
+  if (q == nullptr || softmax_lse == nullptr || out == nullptr) return SMLA_ERR_NULLPTR;
+  if (g.k_rows > 0 && k == nullptr) return SMLA_ERR_NULLPTR;
+  if (g.sparse && sparse_indices == nullptr) return SMLA_ERR_NULLPTR;
+  if (plan->desc.has_topk_length && topk_length == nullptr) return SMLA_ERR_NULLPTR;
+  if (!aligned16(q) || (k != nullptr && !aligned16(k)) || !aligned4(softmax_lse) || !aligned4(out) ||
+      (sparse_indices != nullptr && !aligned4(sparse_indices)) || (topk_length != nullptr && !aligned4(topk_length)))
+    return SMLA_ERR_INVALID;
+
+  CUtensorMap tq, tk;
+  const int q_box = g.R * g.G;
+  if (!encode_rows_map(&tq, q, g.q_rows, q_box, plan->desc.dtype)) {
+    g_last_cuda_error = "cuTensorMapEncodeTiled(q) failed";
+    return SMLA_ERR_CUDA;
+  }
+  if (g.k_rows > 0) {
+    if (!encode_rows_map(&tk, k, g.k_rows, g.sparse ? 1 : smla::kTileKeys, plan->desc.dtype)) {
+      g_last_cuda_error = "cuTensorMapEncodeTiled(k) failed";
+      return SMLA_ERR_CUDA;
+    }
+  } else {
+    tk = tq;  // no key row exists: every item has zero tiles and k is never read
+  }
+  smla::KernelParams p{};
+  p.items = plan->d_items;
+  p.cta_begin = plan->d_cta_begin;
+  p.status = plan->d_status;
+  p.lse = softmax_lse;
+  p.idx = g.sparse ? sparse_indices : nullptr;
+  p.topk_len = plan->desc.has_topk_length ? topk_length : nullptr;
+  p.out = out;
+  p.G = g.G;
+  p.R = g.R;
+  p.n_mma = g.n_mma;
+  p.q_box_rows = q_box;
+  p.topk = g.sparse ? plan->desc.topk : 0;
+  p.width = g.width;
+  p.mask_mode = plan->desc.mask_mode;
+  p.stages = plan->stages;
+  p.idesc = static_cast<int32_t>(plan->idesc);
+  p.c_log2 = static_cast<float>(static_cast<double>(plan->desc.softmax_scale) * 1.4426950408889634);
+  p.inv_g = 1.0f / static_cast<float>(g.G);
+  p.timeout_ns = plan->timeout_ns;
+  cudaError_t e = smla::launch_fused(p, tq, tk, g.sparse, plan->num_ctas, plan->smem,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return SMLA_OK;
+}
+
+smla_status smla_l1norm_run_from_host(const smla_plan* plan, const void* h_q, const void* h_k, const float* h_lse,
+                                      const int32_t* h_indices, const int32_t* h_topk_length, float* h_out,
+                                      void* d_q, void* d_k, float* d_lse, int32_t* d_indices,
+                                      int32_t* d_topk_length, float* d_out, smla_stream_t stream) {
+  if (plan == nullptr) return SMLA_ERR_NULLPTR;
+  smla_io_sizes s;
+  smla_l1norm_io_sizes(plan, &s);
+  auto st = reinterpret_cast<cudaStream_t>(stream);
+  struct Copy {
+    void* dst;
+    const void* src;
+    size_t n;
+  } copies[5] = {{d_q, h_q, s.q_bytes},
+                 {d_k, h_k, s.k_bytes},
+                 {d_lse, h_lse, s.lse_bytes},
+                 {d_indices, h_indices, s.indices_bytes},
+                 {d_topk_length, h_topk_length, s.topk_length_bytes}};
+  if (s.out_bytes > 0 && (h_out == nullptr || d_out == nullptr)) return SMLA_ERR_NULLPTR;
+  for (const Copy& c : copies) {
+    if (c.n == 0) continue;
+    if (c.dst == nullptr || c.src == nullptr) return SMLA_ERR_NULLPTR;
+  }
+  for (const Copy& c : copies) {
+    if (c.n == 0) continue;
+    cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(H2D)");
+  }
+  smla_status r = smla_l1norm_run(plan, d_q, d_k, d_lse, d_indices, d_topk_length, d_out, stream);
+  if (r != SMLA_OK) return r;
+  if (s.out_bytes > 0) {
+    cudaError_t e = cudaMemcpyAsync(h_out, d_out, s.out_bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(D2H)");
+  }
+  return SMLA_OK;
+}
+
+smla_status smla_l1norm_get_status(const smla_plan* plan, smla_stream_t stream, int32_t* flags) {
+  if (plan == nullptr) return SMLA_ERR_NULLPTR;
+  auto st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, plan->d_status, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(plan->d_status, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "get_status");
+  if (flags != nullptr) *flags = v;
+  if (v & smla::kFlagTimeout) return SMLA_ERR_TIMEOUT;
+  if (v & smla::kFlagBadIndex) return SMLA_WARN_BAD_INDEX;
+  return SMLA_OK;
+}
+
+// Test hook: run a bounded wait on a barrier that nothing completes and
+// report the status it leaves (SMLA_ERR_TIMEOUT when the bound works).
+smla_status smla_debug_wait_timeout_probe(int64_t timeout_ns, smla_stream_t stream, int32_t* flags) {
+  int32_t* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, sizeof(int32_t));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(probe)");
+  auto st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  e = cudaMemsetAsync(d, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = smla::launch_wait_timeout_probe(d, timeout_ns, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&v, d, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaFree(d);
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe");
+  if (flags != nullptr) *flags = v;
+  return (v & smla::kFlagTimeout) ? SMLA_ERR_TIMEOUT : SMLA_OK;
+}
+
+const char* smla_status_string(smla_status s) {
+  switch (s) {
+    case SMLA_OK: return "SMLA_OK";
+    case SMLA_ERR_NULLPTR: return "SMLA_ERR_NULLPTR: a required pointer is NULL";
+    case SMLA_ERR_INVALID: return "SMLA_ERR_INVALID: shape, layout, dtype or constraint violated";
+    case SMLA_ERR_UNSUPPORTED: return "SMLA_ERR_UNSUPPORTED: documented feature not built (cmp_ratio != 1, mask modes 1/2)";
+    case SMLA_ERR_CUDA: return "SMLA_ERR_CUDA: a CUDA call failed";
+    case SMLA_ERR_TIMEOUT: return "SMLA_ERR_TIMEOUT: a device-side wait gave up";
+    case SMLA_WARN_BAD_INDEX: return "SMLA_WARN_BAD_INDEX: a sparse index outside [-1, Sk) was treated as masked";
+  }
+  return "unknown smla_status";
+}
+
+const char* smla_get_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+}  // extern "C"

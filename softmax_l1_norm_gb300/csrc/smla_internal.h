@@ -1,0 +1,81 @@
+// Internal structures shared by the host API (smla_api.cpp) and the kernel
+// (smla_kernel.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace smla {
+
+// Head dimension fixed by the operator's constraints (D = 512).
+constexpr int kHeadDim = 512;
+// Keys per MMA tile (the M of one tcgen05.mma; one TMEM lane per key).
+constexpr int kTileKeys = 128;
+// Head-dimension slice per shared-memory stage: 64 half values = 128 bytes,
+// one SWIZZLE_128B row.
+constexpr int kChunkElems = 64;
+constexpr int kNumChunks = kHeadDim / kChunkElems;  // 8
+constexpr int kKStageBytes = kTileKeys * kChunkElems * 2;  // 16 KB
+// TMEM accumulators: 4 buffers of 128 fp32 columns (all 512 columns).
+constexpr int kAccBufs = 4;
+constexpr int kAccCols = 128;
+constexpr int kMaxStages = 8;
+constexpr int kThreads = 384;  // 12 warps: producer, MMA, 2 spare, 2 epilogue warpgroups
+
+// Status word bits.
+constexpr int kFlagBadIndex = 1;
+constexpr int kFlagTimeout = 2;
+
+// One unit of work: one query token (sparse form) or R consecutive tokens of
+// one sequence (dense form).  32 bytes.
+struct WorkItem {
+  int32_t q_tok;    // first query token (global index: b*S1 + r or cu_q[b] + r)
+  int32_t nrows;    // tokens in this item (1 when sparse)
+  int32_t r0;       // local row of q_tok within its sequence
+  int32_t k_base;   // global key row of key position 0 of the sequence
+  int32_t Sq;       // query length of the sequence
+  int32_t Sk;       // key length of the sequence
+  int32_t ntiles;   // dense form: 128-key tiles to compute (the rest is zero)
+  int32_t pad;
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem is 32 bytes");
+
+struct KernelParams {
+  const WorkItem* items;
+  const int32_t* cta_begin;   // [gridDim.x + 1]
+  int32_t* status;
+  const float* lse;           // (tokens, G)
+  const int32_t* idx;         // (tokens, topk) or null
+  const int32_t* topk_len;    // (tokens) or null
+  float* out;                 // (tokens, width)
+  int32_t G;                  // heads per key head
+  int32_t R;                  // tokens per item (dense), 1 (sparse)
+  int32_t n_mma;              // MMA N = pad16(R*G)
+  int32_t q_box_rows;         // rows of q one TMA box moves (= R*G)
+  int32_t topk;               // 0 = dense
+  int32_t width;              // output row length
+  int32_t mask_mode;          // 0 or 3
+  int32_t stages;             // key ring depth
+  int32_t idesc;              // tcgen05 instruction descriptor
+  float c_log2;               // softmax_scale * log2(e)
+  float inv_g;                // 1 / G
+  int64_t timeout_ns;         // bound on every device-side wait
+};
+
+// Shared-memory footprint for a given MMA N and ring depth.
+inline int smem_bytes_for(int n_mma, int stages) {
+  const int q_bytes = kNumChunks * n_mma * 128;
+  const int ring = stages * kKStageBytes;
+  const int bars = (2 * kNumChunks + 2 * kMaxStages + 2 * kAccBufs + 2) * 8;
+  const int tables = 2 * kAccCols * 4;  // per-warpgroup lse table
+  return 1024 /* alignment slack */ + q_bytes + ring + bars + tables + 64;
+}
+
+// Launch the fused kernel (defined in smla_kernel.cu).
+cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                         bool sparse, int grid, int smem_bytes, cudaStream_t stream);
+cudaError_t configure_fused(int smem_bytes);
+
+}  // namespace smla

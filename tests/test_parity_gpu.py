@@ -1,0 +1,198 @@
+"""GPU parity: the CUDA library against the fp64 oracle, element by element,
+through the C ABI.  Tolerance |gpu - oracle| <= 1e-5 + 2e-3 |oracle|; row sums
+within 1e-3 of 1 where the LSE is the exact forward LSE."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from smla_harness import (ROWSUM_TOL, assert_close, exact_lse, invalid_slot_mask, oracle_kwargs,
+                          plan_kwargs, run_gpu, to_device)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+def full_parity(smla, w, check_rowsum=True, **plan_extra):
+    exact_lse(oracle, w)
+    got, plan, t, status = run_gpu(smla, w, **plan_extra)
+    want = oracle.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **oracle_kwargs(w))
+    assert got.shape == want.shape
+    assert_close(got, want, what=w.name)
+    rows = got.reshape(w.n_tokens, -1).astype(np.float64)
+    bad = invalid_slot_mask(w)
+    assert np.all(rows[bad] == 0.0), "masked / padding slots must be exactly 0"
+    if check_rowsum:
+        lse = w.lse_rows()
+        has = ~np.isneginf(lse[:, 0])
+        sums = rows.sum(axis=1)
+        assert np.all(np.abs(sums[has] - 1.0) <= ROWSUM_TOL), f"row sums {sums[has].min()}..{sums[has].max()}"
+        assert np.all(sums[~has] == 0.0)
+    return got, plan, status
+
+
+def test_config1_tiny_sparse(lib):
+    w = W.make_config(1, lse=None)
+    _, plan, status = full_parity(lib, w)
+    assert status[0] == lib.SMLA_OK
+
+
+def test_config2_dense_causal(lib):
+    w = W.make_config(2, lse=None)
+    _, plan, status = full_parity(lib, w)
+    assert plan.info.rows_per_item == 8 and status[0] == lib.SMLA_OK
+
+
+@pytest.mark.parametrize("G", [1, 3, 8, 16, 24, 64, 100, 128])
+def test_sparse_head_counts_multi_tile_ragged(lib, G):
+    """Several 128-key tiles plus a ragged tail (topk 300), causal, bf16."""
+    w = W.make_workload(layout="BSND", dtype="bf16", B=2, S1=24, S2=700, G=G, topk=300,
+                        mask_mode=3, seed=1000 + G, lse=None)
+    full_parity(lib, w)
+
+
+@pytest.mark.parametrize("G", [1, 5, 16, 48, 128])
+def test_dense_head_counts(lib, G):
+    """Dense form: R = 128 // G tokens packed per MMA, causal with S1 < S2."""
+    w = W.make_workload(layout="BSND", dtype="fp16", B=2, S1=37, S2=300, G=G, topk=0,
+                        mask_mode=3, seed=2000 + G, lse=None)
+    full_parity(lib, w)
+
+
+def test_dense_no_mask_bf16(lib):
+    w = W.make_workload(layout="BSND", dtype="bf16", B=1, S1=20, S2=257, G=8, topk=0,
+                        mask_mode=0, seed=2100, lse=None)
+    full_parity(lib, w)
+
+
+def test_tnd_sparse_varlen(lib):
+    w = W.make_workload(layout="TND", dtype="fp16", seqlens_q=[130, 1, 0, 77, 260],
+                        seqlens_k=[130, 5, 3, 200, 260], G=64, topk=256, mask_mode=3,
+                        seed=2200, lse=None)
+    full_parity(lib, w)
+
+
+def test_tnd_dense_width_beyond_sequences(lib):
+    w = W.make_workload(layout="TND", dtype="bf16", seqlens_q=[40, 9, 70],
+                        seqlens_k=[50, 9, 130], G=16, topk=0, mask_mode=3, max_seqlen_k=150,
+                        seed=2300, lse=None)
+    full_parity(lib, w)
+
+
+def test_s1_longer_than_s2_rows_without_keys(lib):
+    w = W.make_workload(layout="BSND", dtype="bf16", B=1, S1=40, S2=16, G=8, topk=0,
+                        mask_mode=3, seed=2400, lse=None)
+    got, _, _ = full_parity(lib, w)
+    assert np.all(got.reshape(40, -1)[:24] == 0.0)
+
+
+def test_bad_indices_are_masked_and_reported(lib):
+    """No topk_length: every slot is a candidate; -1 is padding, other values
+    outside [0, Sk) are masked and raise the bad-index warning."""
+    w = W.make_workload(layout="BSND", dtype="fp16", B=2, S1=6, S2=300, G=16, topk=200,
+                        mask_mode=3, seed=2500, lse=None, with_topk_length=False)
+    rng = np.random.Generator(np.random.PCG64(2500))
+    w.sparse_indices = rng.integers(-3, 330, size=w.sparse_indices.shape).astype(np.int32)
+    _, _, status = full_parity(lib, w)
+    assert status[0] == lib.SMLA_WARN_BAD_INDEX and (status[1] & 1)
+
+
+def test_topk_length_clamped_and_zero(lib):
+    w = W.make_workload(layout="BSND", dtype="bf16", B=1, S1=8, S2=512, G=32, topk=256,
+                        mask_mode=0, seed=2600, lse=None)
+    tl = w.topk_length.reshape(-1)
+    tl[:] = [0, -5, 1, 255, 256, 999, 128, 129]
+    # the oracle reads topk_length as "slot < topk_length"; clamping to [0, topk] is the same
+    full_parity(lib, w)
+
+
+def test_empty_q_returns_at_once(lib):
+    plan = lib.Plan(layout="BSND", dtype="bf16", num_heads_q=8, batch_size=0, max_seqlen_q=16,
+                    max_seqlen_k=64, topk=8, mask_mode=0, softmax_scale=1.0)
+    assert plan.output_shape == (0, 16, 1, 8)
+    code = plan._lib.smla_l1norm_run(plan._h, None, None, None, None, None, None, None)
+    assert code == lib.SMLA_OK
+
+
+def test_deterministic_bitwise(lib):
+    w = W.make_workload(layout="BSND", dtype="bf16", B=1, S1=200, S2=2048, G=128, topk=1024,
+                        mask_mode=3, seed=2700)
+    a, plan, t, _ = run_gpu(lib, w)
+    b, _, _, _ = run_gpu(lib, w, plan=plan, tensors=t)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    # another grid size gives the same bits (the schedule only moves work)
+    c, _, _, _ = run_gpu(lib, w, tensors=t, num_ctas=7)
+    assert np.array_equal(a.view(np.uint32), c.view(np.uint32))
+
+
+def test_run_from_host_matches_run(lib):
+    w = W.make_config(1)
+    a, plan, t, _ = run_gpu(lib, w)
+    pin = {k: (None if v is None else v.cpu().pin_memory()) for k, v in
+           {"q": t["q"], "k": t["k"], "lse": t["lse"], "indices": t["idx"], "topk_length": t["tl"]}.items()}
+    pin["out"] = torch.empty(plan.output_shape, dtype=torch.float32).pin_memory()
+    dev = {"q": torch.empty_like(t["q"]), "k": torch.empty_like(t["k"]), "lse": torch.empty_like(t["lse"]),
+           "indices": torch.empty_like(t["idx"]), "topk_length": torch.empty_like(t["tl"]),
+           "out": torch.empty(plan.output_shape, dtype=torch.float32, device="cuda")}
+    plan.run_from_host(pin, dev)
+    torch.cuda.synchronize()
+    assert np.array_equal(pin["out"].numpy(), a)
+
+
+def test_functional_api_matches_plan(lib):
+    w = W.make_workload(layout="TND", dtype="bf16", seqlens_q=[33, 70], seqlens_k=[33, 90], G=16,
+                        topk=64, mask_mode=3, seed=2800)
+    a, _, t, _ = run_gpu(lib, w)
+    b = lib.sparse_flash_mla_softmax_l1_norm(
+        t["q"], t["k"], t["lse"], sparse_indices=t["idx"], topk_length=t["tl"],
+        cu_seqlens_q=w.cu_seqlens_q, cu_seqlens_k=w.cu_seqlens_k, softmax_scale=w.softmax_scale,
+        mask_mode=3, layout_q="TND", layout_k="TND")
+    assert np.array_equal(b.cpu().numpy(), a)
+
+
+def test_wait_timeout_probe_reports_and_returns(lib):
+    code, flags = lib.wait_timeout_probe(50_000_000)
+    assert code == lib.SMLA_ERR_TIMEOUT and (flags & 2)
+    # the context is still usable afterwards
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum()) == 4.0
+
+
+# ---------------------------------------------------------------- full sizes
+def sampled_parity(lib, n, n_sample=24, seed=0):
+    """Full-size configuration, in the launch configuration the benchmark
+    times.  Exact LSE is planted for a sample of rows, which are compared
+    element by element with the oracle and must sum to 1; every row is
+    checked for exact zeros on invalid slots and for finite, non-negative
+    values."""
+    w = W.make_config(n)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n_tok = w.n_tokens
+    rows = sorted(set([0, 1, n_tok - 1, n_tok // 2] + rng.choice(n_tok, n_sample, replace=False).tolist()))
+    exact_lse(oracle, w, rows=rows)
+    got, plan, t, status = run_gpu(lib, w)
+    assert status[0] == lib.SMLA_OK
+    got_rows = got.reshape(n_tok, -1)
+    want = oracle.softmax_l1_norm_rows(w.q_bits, w.k_bits, w.softmax_lse, rows, **oracle_kwargs(w))
+    assert_close(got_rows[rows], want, what=f"config {n} sampled rows")
+    sums = got_rows[rows].astype(np.float64).sum(axis=1)
+    assert np.all(np.abs(sums - 1.0) <= ROWSUM_TOL), sums
+    assert np.all(np.isfinite(got_rows)) and np.all(got_rows >= 0)
+    bad = invalid_slot_mask(w)
+    assert np.all(got_rows[bad] == 0.0)
+    return w, got_rows
+
+
+def test_config3_dsv32_full_size_sampled(lib):
+    sampled_parity(lib, 3)
+
+
+def test_config4_varlen_tnd_full_size_sampled(lib):
+    sampled_parity(lib, 4)
+
+
+def test_config5_long_clustered_full_size_sampled(lib):
+    sampled_parity(lib, 5, n_sample=16)
