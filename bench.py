@@ -265,7 +265,7 @@ def run_reference(args, world, rank):
     rows = sum(s[0] for s in r["steps"])
     pairs = sum(s[1] for s in r["steps"])
     secs = sum(s[2] for s in r["steps"])
-    name = W.config_names()[args.config]
+    name = W.CONFIG_NAMES[args.config]
     value = pairs / secs
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -293,7 +293,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(device)
 
     w = W.make_config(args.config)
-    name = W.config_names()[args.config]
+    name = w.name
     pairs, flops, bytes_ = workload_numbers(w)
     alg_bytes = sum(bytes_.values())
 

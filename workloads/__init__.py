@@ -38,7 +38,7 @@ import numpy as np
 HEAD_DIM = 512  # the only head size the operator supports (约束说明: D 仅支持 512)
 
 __all__ = [
-    "Workload", "CONFIGS", "config_names", "make_config", "make_workload",
+    "Workload", "CONFIGS", "CONFIG_NAMES", "config_names", "make_config", "make_workload",
     "bf16_bits_from_f32", "half_bits_to_f32", "visible_count", "lse_estimate",
     "default_scale",
 ]
@@ -402,18 +402,27 @@ def set_lse_rows(w: Workload, rows: np.ndarray) -> None:
 # ----------------------------------------------------------------------------
 # the five named configurations
 # ----------------------------------------------------------------------------
+CONFIG_NAMES = {
+    1: "tiny_sparse_B1_S16_S2_256_G8_topk32",
+    2: "dense_causal_B2_S512_G16",
+    3: "dsv32_sparse_causal_S4096_G128_topk2048",
+    4: "varlen_tnd_8seq_G64_topk2048",
+    5: "long_clustered_S32768_G128_topk2048",
+}
+
+
 def _cfg_tiny_sparse(lse="estimate"):
-    return make_workload(name="tiny_sparse_B1_S16_S2_256_G8_topk32", layout="BSND", dtype="bf16",
+    return make_workload(name=CONFIG_NAMES[1], layout="BSND", dtype="bf16",
                          B=1, S1=16, S2=256, G=8, topk=32, mask_mode=0, seed=1, lse=lse)
 
 
 def _cfg_dense_causal(lse="estimate"):
-    return make_workload(name="dense_causal_B2_S512_G16", layout="BSND", dtype="fp16",
+    return make_workload(name=CONFIG_NAMES[2], layout="BSND", dtype="fp16",
                          B=2, S1=512, S2=512, G=16, topk=0, mask_mode=3, seed=2, lse=lse)
 
 
 def _cfg_dsv32(lse="estimate"):
-    return make_workload(name="dsv32_sparse_causal_S4096_G128_topk2048", layout="BSND",
+    return make_workload(name=CONFIG_NAMES[3], layout="BSND",
                          dtype="bf16", B=1, S1=4096, S2=4096, G=128, topk=2048, mask_mode=3,
                          seed=3, lse=lse)
 
@@ -421,13 +430,13 @@ def _cfg_dsv32(lse="estimate"):
 def _cfg_varlen_tnd(lse="estimate"):
     rng = np.random.Generator(np.random.PCG64(4))
     lens = rng.integers(512, 8192, size=8, endpoint=True)
-    return make_workload(name="varlen_tnd_8seq_G64_topk2048", layout="TND", dtype="fp16",
+    return make_workload(name=CONFIG_NAMES[4], layout="TND", dtype="fp16",
                          seqlens_q=lens, seqlens_k=lens, G=64, topk=2048, mask_mode=3,
                          seed=4, rng=rng, lse=lse)
 
 
 def _cfg_long_clustered(lse="estimate"):
-    return make_workload(name="long_clustered_S32768_G128_topk2048", layout="BSND", dtype="bf16",
+    return make_workload(name=CONFIG_NAMES[5], layout="BSND", dtype="bf16",
                          B=1, S1=32768, S2=32768, G=128, topk=2048, mask_mode=3,
                          index_mode="clustered", seed=5, lse=lse)
 
@@ -442,7 +451,7 @@ CONFIGS = {
 
 
 def config_names():
-    return {k: v.__name__[5:] for k, v in CONFIGS.items()}
+    return dict(CONFIG_NAMES)
 
 
 def make_config(n: int, lse="estimate") -> Workload:
