@@ -61,8 +61,10 @@ typedef enum {
                                 cmp_ratio != 1, mask modes other than 0 and 3     */
   SMLA_ERR_CUDA = 4,         /* a CUDA runtime call failed (see get_last_cuda_error) */
   SMLA_ERR_TIMEOUT = 5,      /* a device-side wait gave up (reported by get_status) */
-  SMLA_WARN_BAD_INDEX = 6    /* a sparse index outside [-1, Sk) was seen and treated
+  SMLA_WARN_BAD_INDEX = 6,   /* a sparse index outside [-1, Sk) was seen and treated
                                 as masked (reported by get_status)                 */
+  SMLA_ERR_CAPACITY = 7      /* smla_l1norm_run_noalloc: the problem needs more work
+                                items than its fixed scratch holds                 */
 } smla_status;
 
 typedef enum { SMLA_LAYOUT_BSND = 0, SMLA_LAYOUT_TND = 1 } smla_layout;
@@ -238,6 +240,45 @@ smla_status smla_l1norm_schedule_host(const smla_l1norm_desc *desc, int32_t num_
  * bound works.  Allocates and frees 4 bytes of device memory.
  */
 smla_status smla_debug_wait_timeout_probe(int64_t timeout_ns, smla_stream_t stream, int32_t *flags);
+
+/*
+ * Allocation-free form of smla_l1norm_run() (the article has no counterpart;
+ * the operator is the same).  For callers that cannot call cudaMalloc: code
+ * running where a framework's caching allocator owns all device memory, a
+ * plugin that is handed device pointers but no allocator, a service that
+ * forbids allocation after start-up.  No plan is needed: pass the
+ * description and the same tensors as smla_l1norm_run().
+ *
+ * Scratch: the work list and the status word live in a fixed file-scope
+ * device array of 2,101,760 bytes (2 MiB of work items plus offsets and the
+ * status word), which every GPU that loads this library holds until the
+ * process exits.  Capacity: at most 65,536 work items (query tokens in the
+ * sparse form; packs of 128/G tokens in the dense form) and 1,024 CTAs;
+ * larger problems return SMLA_ERR_CAPACITY before any CUDA call.
+ *
+ * The call allocates nothing: no cudaMalloc / cudaFree, no allocating CUDA
+ * or torch routine, no host heap.  It builds the work list in fixed host
+ * staging memory, copies it into the device array with cudaMemcpyAsync on
+ * ``stream`` (from pageable memory, so the call waits for the stream's
+ * earlier work before the copy starts), and launches the fused kernel.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the device address of the scratch array with cudaGetSymbolAddress and
+ * caches it; make that first call before any stream capture.
+ *
+ * Sharing: all calls on a device use the same array, which keeps the last
+ * call's contents; each call rewrites the work list and clears the status
+ * word.  Calls that overlap on the GPU (issued on different streams, or from
+ * several host threads) race on the array: serialise them.  Device-side flags
+ * (bad index, wait timeout) are recorded in the array's status word but not
+ * reported; use the plan-based path to read them.
+ *
+ * Returns SMLA_OK, the validation codes of smla_l1norm_plan_create /
+ * smla_l1norm_run, SMLA_ERR_CAPACITY, or SMLA_ERR_CUDA.
+ */
+smla_status smla_l1norm_run_noalloc(const smla_l1norm_desc *desc, const void *q, const void *k,
+                                    const float *softmax_lse, const int32_t *sparse_indices,
+                                    const int32_t *topk_length, float *out, smla_stream_t stream);
 
 /* Static description of a status code. */
 const char *smla_status_string(smla_status status);

@@ -24,12 +24,13 @@ from . import build as _build
 
 __all__ = [
     "SMLA_OK", "SMLA_ERR_NULLPTR", "SMLA_ERR_INVALID", "SMLA_ERR_UNSUPPORTED", "SMLA_ERR_CUDA",
-    "SMLA_ERR_TIMEOUT", "SMLA_WARN_BAD_INDEX", "SmlaError", "Plan", "library", "library_path",
-    "sparse_flash_mla_softmax_l1_norm", "schedule_host", "wait_timeout_probe",
+    "SMLA_ERR_TIMEOUT", "SMLA_WARN_BAD_INDEX", "SMLA_ERR_CAPACITY", "SmlaError", "Plan", "library",
+    "library_path", "sparse_flash_mla_softmax_l1_norm", "schedule_host", "wait_timeout_probe",
+    "run_noalloc",
 ]
 
 SMLA_OK, SMLA_ERR_NULLPTR, SMLA_ERR_INVALID, SMLA_ERR_UNSUPPORTED = 0, 1, 2, 3
-SMLA_ERR_CUDA, SMLA_ERR_TIMEOUT, SMLA_WARN_BAD_INDEX = 4, 5, 6
+SMLA_ERR_CUDA, SMLA_ERR_TIMEOUT, SMLA_WARN_BAD_INDEX, SMLA_ERR_CAPACITY = 4, 5, 6, 7
 LAYOUTS = {"BSND": 0, "TND": 1}
 DTYPES = {"fp16": 0, "float16": 0, "bf16": 1, "bfloat16": 1}
 
@@ -115,6 +116,8 @@ def library():
     lib.smla_status_string.restype = ctypes.c_char_p
     lib.smla_get_last_cuda_error.argtypes = []
     lib.smla_get_last_cuda_error.restype = ctypes.c_char_p
+    lib.smla_l1norm_run_noalloc.argtypes = [ctypes.POINTER(_Desc), P, P, P, P, P, P, P]
+    lib.smla_l1norm_run_noalloc.restype = I32
     lib.smla_debug_wait_timeout_probe.argtypes = [I64, P, ctypes.POINTER(I32)]
     lib.smla_debug_wait_timeout_probe.restype = I32
     _ = F32
@@ -289,6 +292,23 @@ def wait_timeout_probe(timeout_ns: int = 50_000_000, stream=None):
     if code not in (SMLA_OK, SMLA_ERR_TIMEOUT):
         _check(code, "smla_debug_wait_timeout_probe")
     return code, flags.value
+
+
+def run_noalloc(q, k, softmax_lse, out, sparse_indices=None, topk_length=None, stream=None,
+                **desc_kwargs):
+    """``smla_l1norm_run_noalloc``: the allocation-free entry point, for
+    callers that cannot allocate device memory.  ``out`` must be given (this
+    path allocates nothing); its scratch is a fixed device array shared by all
+    calls on the device, so calls must not overlap on the GPU."""
+    lib = library()
+    d, keep = _make_desc(**desc_kwargs)
+    code = lib.smla_l1norm_run_noalloc(
+        ctypes.byref(d), _ptr(q, "q"), _ptr(k, "k", required=False), _ptr(softmax_lse, "softmax_lse"),
+        _ptr(sparse_indices, "sparse_indices", required=False),
+        _ptr(topk_length, "topk_length", required=False), _ptr(out, "out"), _stream_handle(stream))
+    del keep
+    _check(code, "smla_l1norm_run_noalloc")
+    return out
 
 
 _PLAN_CACHE = {}

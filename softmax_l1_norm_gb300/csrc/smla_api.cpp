@@ -591,6 +591,8 @@ const char* smla_status_string(smla_status s) {
     case SMLA_ERR_CUDA: return "SMLA_ERR_CUDA: a CUDA call failed";
     case SMLA_ERR_TIMEOUT: return "SMLA_ERR_TIMEOUT: a device-side wait gave up";
     case SMLA_WARN_BAD_INDEX: return "SMLA_WARN_BAD_INDEX: a sparse index outside [-1, Sk) was treated as masked";
+    case SMLA_ERR_CAPACITY:
+      return "SMLA_ERR_CAPACITY: smla_l1norm_run_noalloc holds at most 65536 work items and 1024 CTAs";
   }
   return "unknown smla_status";
 }
