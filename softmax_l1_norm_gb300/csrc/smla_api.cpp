@@ -473,21 +473,14 @@ smla_status smla_l1norm_run(const smla_plan* plan, const void* q, const void* k,
       (sparse_indices != nullptr && !aligned4(sparse_indices)) || (topk_length != nullptr && !aligned4(topk_length)))
     return SMLA_ERR_INVALID;
 
-  CUtensorMap tq, tk;
+  CUtensorMap tq;
   const int q_box = g.R * g.G;
   if (!encode_rows_map(&tq, q, g.q_rows, q_box, plan->desc.dtype)) {
     g_last_cuda_error = "cuTensorMapEncodeTiled(q) failed";
     return SMLA_ERR_CUDA;
   }
-  if (g.k_rows > 0) {
-    if (!encode_rows_map(&tk, k, g.k_rows, g.sparse ? 1 : smla::kTileKeys, plan->desc.dtype)) {
-      g_last_cuda_error = "cuTensorMapEncodeTiled(k) failed";
-      return SMLA_ERR_CUDA;
-    }
-  } else {
-    tk = tq;  // no key row exists: every item has zero tiles and k is never read
-  }
   smla::KernelParams p{};
+  p.k = static_cast<const uint8_t*>(k);  // unread when there is no key row (every item has zero tiles)
   p.items = plan->d_items;
   p.cta_begin = plan->d_cta_begin;
   p.status = plan->d_status;
@@ -507,7 +500,7 @@ smla_status smla_l1norm_run(const smla_plan* plan, const void* q, const void* k,
   p.c_log2 = static_cast<float>(static_cast<double>(plan->desc.softmax_scale) * 1.4426950408889634);
   p.inv_g = 1.0f / static_cast<float>(g.G);
   p.timeout_ns = plan->timeout_ns;
-  cudaError_t e = smla::launch_fused(p, tq, tk, g.sparse, plan->num_ctas, plan->smem,
+  cudaError_t e = smla::launch_fused(p, tq, g.sparse, plan->num_ctas, plan->smem,
                                      reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return SMLA_OK;

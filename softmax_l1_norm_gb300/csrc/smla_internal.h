@@ -22,7 +22,7 @@ constexpr int kKStageBytes = kTileKeys * kChunkElems * 2;  // 16 KB
 constexpr int kAccBufs = 4;
 constexpr int kAccCols = 128;
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 384;  // 12 warps: producer, MMA, 2 spare, 2 epilogue warpgroups
+constexpr int kThreads = 512;  // 16 warps: 4 key producers, MMA, q loader, 2 spare, 2 epilogue warpgroups
 
 // Status word bits.
 constexpr int kFlagBadIndex = 1;
@@ -43,6 +43,7 @@ struct WorkItem {
 static_assert(sizeof(WorkItem) == 32, "WorkItem is 32 bytes");
 
 struct KernelParams {
+  const uint8_t* k;           // key rows, 1024 bytes each
   const WorkItem* items;
   const int32_t* cta_begin;   // [gridDim.x + 1]
   int32_t* status;
@@ -74,8 +75,8 @@ inline int smem_bytes_for(int n_mma, int stages) {
 }
 
 // Launch the fused kernel (defined in smla_kernel.cu).
-cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
-                         bool sparse, int grid, int smem_bytes, cudaStream_t stream);
+cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int grid,
+                         int smem_bytes, cudaStream_t stream);
 cudaError_t configure_fused(int smem_bytes);
 
 }  // namespace smla

@@ -7,17 +7,22 @@
 //     out[i] = 0                                                   otherwise
 // with j_i = sparse_indices[i] (stage 1 gather) or j_i = i (dense form).
 //
-// How (one persistent CTA per SM, 384 threads, warp-specialised):
-//   warp 0      producer.  TMA loads the token's q block (G heads x 512) into
-//               8 shared-memory chunks of 64 columns (SWIZZLE_128B), and
-//               streams the selected key rows through a ring of 16 KB stages
-//               (128 keys x 64 columns): tile::gather4 TMA for sparse
-//               indices (4 arbitrary rows per instruction, one instruction
-//               per lane), a plain tiled TMA for the dense form.
-//   warp 1      MMA issuer.  tcgen05.mma kind::f16, M = 128 keys (A = key
+// How (one persistent CTA per SM, 512 threads, warp-specialised):
+//   warps 0-3   key producers.  Each 128-key tile is moved in 8 stages of
+//               64 head-dim columns (128 keys x 128 bytes = 16 KB).  Every
+//               thread copies 16-byte pieces with cp.async straight into the
+//               128-byte-swizzle position the MMA descriptor expects (a warp
+//               instruction covers 4 whole 128-byte key rows), so any key
+//               order costs the same as a contiguous tile.  The key indices
+//               of the next tile are fetched while the current tile streams.
+//   warp 4      MMA issuer.  tcgen05.mma kind::f16, M = 128 keys (A = key
 //               stage), N = G heads padded to 16 (B = q chunk), K = 512 in
 //               32 steps of 16, fp32 accumulation in one of 4 TMEM buffers.
-//   warps 4-11  two epilogue warpgroups taking alternate tiles.  Thread t
+//   warp 5      q loader.  TMA loads each token's q block (G heads x 512) as
+//               8 chunks of 64 columns (SWIZZLE_128B); chunk c of the next
+//               token loads as soon as the last MMA of the current token has
+//               read chunk c.
+//   warps 8-15  two epilogue warpgroups taking alternate tiles.  Thread t
 //               owns TMEM lane t, i.e. key slot t of the tile, reads its G
 //               accumulator columns, and sums exp2(s*scale*log2e - lse*log2e)
 //               over the heads in registers: the head reduction needs no
@@ -76,23 +81,30 @@ struct WaitCtl {
   int64_t timeout_ns;
 };
 
-// Wait for the phase with the given parity to complete, for at most
-// ctl.timeout_ns, or until another role has given up.  Returns false on
-// either; a timeout sets the abort flag and the status bit.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of a bounded wait: poll until the phase completes, another role
+// gave up, or the time limit passes (then set the abort flag and status bit).
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int32_t* abort,
+                                       int32_t* status, int64_t timeout_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
-      if (*ctl.abort) return false;
-      if (global_timer_ns() - t0 > static_cast<uint64_t>(ctl.timeout_ns)) {
-        *ctl.abort = 1;
-        atomicOr(ctl.status, kFlagTimeout);
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > static_cast<uint64_t>(timeout_ns)) {
+        *abort = 1;
+        atomicOr(status, kFlagTimeout);
         return false;
       }
     }
   }
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// ctl.timeout_ns, or until another role has given up.  Returns false on
+// either.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, ctl.abort, ctl.status, ctl.timeout_ns);
 }
 
 // Same, ignoring the abort flag: used after an abort to let copies and MMAs
@@ -105,7 +117,7 @@ __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, int64_t l
   }
 }
 
-// ---------------------------------------------------------------- TMA
+// ---------------------------------------------------------------- copies
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
   asm volatile(
@@ -114,18 +126,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-// Four whole rows (r0..r3) of a 2-D tensor, columns [x, x+box), into four
-// consecutive 128-byte shared-memory rows; swizzle per the tensor map.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0,
-                                            int r1, int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+// 16 bytes global -> shared, cached in L2 only.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Make this thread's completed generic-proxy shared-memory writes visible to
+// the async proxy (the tensor cores read their operands through it).
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -206,6 +224,15 @@ __device__ __forceinline__ bool wg_all(int id, bool v) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Roles.
+constexpr int kProducerWarps = 4;   // warps 0-3
+constexpr int kMmaWarp = 4;
+constexpr int kQWarp = 5;
+constexpr int kEpiWarp0 = 8;        // warps 8-15
+// A producer thread keeps this many of its stages in flight before it waits
+// for the oldest one and marks it full (must stay below the ring depth).
+constexpr int kCopyLag = 3;
+
 // Key tiles an item needs, and (sparse form) the clamped topk_length.
 template <bool kSparse>
 __device__ __forceinline__ int item_tiles(const KernelParams& p, const WorkItem& w, int& tl) {
@@ -220,13 +247,31 @@ __device__ __forceinline__ int item_tiles(const KernelParams& p, const WorkItem&
   return w.ntiles;
 }
 
+// Position in a CTA's sequence of (item, key tile) pairs, skipping items
+// without tiles.
+struct TileCursor {
+  int it, t, nt, tl;
+  WorkItem w;
+};
+
+template <bool kSparse>
+__device__ __forceinline__ bool cursor_next(const KernelParams& p, TileCursor& c, int it1) {
+  ++c.t;
+  while (c.t >= c.nt) {
+    if (++c.it >= it1) return false;
+    c.w = p.items[c.it];
+    c.nt = item_tiles<kSparse>(p, c.w, c.tl);
+    c.t = 0;
+  }
+  return true;
+}
+
 }  // namespace
 
 template <bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     smla_fused_kernel(const __grid_constant__ KernelParams p,
-                      const __grid_constant__ CUtensorMap tmap_q,
-                      const __grid_constant__ CUtensorMap tmap_k) {
+                      const __grid_constant__ CUtensorMap tmap_q) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -259,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_q_empty + 8 * c, 1);
     }
     for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(bar_k_full + 8 * s, 1);
+      mbar_init(bar_k_full + 8 * s, kProducerWarps * 32);
       mbar_init(bar_k_empty + 8 * s, 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
@@ -277,18 +322,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n16 = kNumChunks * q_chunk_bytes / 16;
     for (int i = threadIdx.x; i < n16; i += blockDim.x) q4[i] = make_uint4(0, 0, 0, 0);
   }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  if (warp == 1) {
+  fence_proxy_async();
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(kAccBufs * kAccCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmap_q);
-    prefetch_tmap(&tmap_k);
-  }
+  if (warp == kQWarp && lane == 0) prefetch_tmap(&tmap_q);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -297,76 +339,110 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int it0 = p.cta_begin[blockIdx.x];
   const int it1 = p.cta_begin[blockIdx.x + 1];
 
-  if (warp == 0) {
-    // ============================================================ producer
-    uint32_t kst = 0, kph = 0, qit = 0;
-    uint32_t k_armed = 0, k_par = 0, q_armed = 0, q_par = 0;  // for the drain on abort
+  if (warp < kProducerWarps) {
+    // ============================================================ key producers
+    // Thread (warp pw, lane l) copies 16-byte segment (l & 7) of key rows
+    // pw*32 + (l >> 3) + 4*i, i = 0..7, of every stage.
+    const int seg = lane & 7;
+    const int krow0 = warp * 32 + (lane >> 3);
+    uint32_t kst = 0, kph = 0;   // ring slot being filled, its phase
+    uint32_t ast = 0;            // ring slot to mark full next
+    uint32_t issued = 0, marked = 0;
     bool ok = true;
-    const uint32_t q_tx = static_cast<uint32_t>(p.q_box_rows) * 128u;
-    for (int it = it0; it < it1 && ok; ++it) {
-      const WorkItem w = p.items[it];
-      int tl;
-      const int nt = item_tiles<kSparse>(p, w, tl);
-      if (nt == 0) continue;
-      const int64_t idx_row = static_cast<int64_t>(w.q_tok) * p.topk;
-      for (int t = 0; t < nt && ok; ++t) {
-        int rows[4] = {0, 0, 0, 0};
-        if (kSparse) {
-          bool bad = false;
+    TileCursor cur{it0 - 1, 0, 0, 0, WorkItem{}};
+    bool have = cursor_next<kSparse>(p, cur, it1);
+    int jn[8];
+    auto fetch_indices = [&](const TileCursor& c) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int slot = t * kTileKeys + lane * 4 + i;
-            int j = -1;
-            if (slot < tl) j = __ldg(p.idx + idx_row + slot);
-            const bool in = (j >= 0) && (j < w.Sk);
-            bad |= (slot < tl) && !in && (j != -1);
-            rows[i] = w.k_base + (in ? j : 0);
-          }
-          if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kFlagBadIndex);
-        }
-        for (int c = 0; c < kNumChunks; ++c) {
-          if (lane == 0) {
-            if (t == 0) {
-              ok = wait_bounded(bar_q_empty + 8 * c, (qit & 1u) ^ 1u, ctl);
-              if (ok) {
-                mbar_arrive_expect_tx(bar_q_full + 8 * c, q_tx);
-                tma_load_2d(sQ + c * q_chunk_bytes, &tmap_q, c * kChunkElems, w.q_tok * p.G,
-                            bar_q_full + 8 * c);
-                q_armed |= 1u << c;
-                q_par = (q_par & ~(1u << c)) | ((qit & 1u) << c);
-              }
-            }
-            if (ok) ok = wait_bounded(bar_k_empty + 8 * kst, kph ^ 1u, ctl);
-            if (ok) mbar_arrive_expect_tx(bar_k_full + 8 * kst, kKStageBytes);
-          }
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          const uint32_t dst = sK + kst * kKStageBytes;
-          if (kSparse) {
-            tma_gather4(dst + lane * 4 * 128, &tmap_k, c * kChunkElems, rows[0], rows[1], rows[2],
-                        rows[3], bar_k_full + 8 * kst);
-          } else if (lane == 0) {
-            tma_load_2d(dst, &tmap_k, c * kChunkElems, w.k_base + t * kTileKeys,
-                        bar_k_full + 8 * kst);
-          }
-          k_armed |= 1u << kst;
-          k_par = (k_par & ~(1u << kst)) | (kph << kst);
-          if (++kst == static_cast<uint32_t>(p.stages)) {
-            kst = 0;
-            kph ^= 1u;
-          }
+      for (int i = 0; i < 8; ++i) {
+        const int slot = c.t * kTileKeys + krow0 + 4 * i;
+        if (kSparse) {
+          jn[i] = slot < c.tl ? __ldg(p.idx + static_cast<int64_t>(c.w.q_tok) * p.topk + slot) : -1;
+        } else {
+          jn[i] = slot;
         }
       }
-      ++qit;
+    };
+    if (have) fetch_indices(cur);
+    while (have && ok) {
+      // source rows of this tile (invalid slots read key 0 of the sequence)
+      const uint8_t* src[8];
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = jn[i];
+        const bool in = (j >= 0) && (j < cur.w.Sk);
+        if (kSparse) bad |= (krow0 + 4 * i + cur.t * kTileKeys < cur.tl) && !in && (j != -1);
+        src[i] = p.k + (static_cast<int64_t>(cur.w.k_base) + (in ? j : 0)) * (kHeadDim * 2) + seg * 16;
+      }
+      if (kSparse && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kFlagBadIndex);
+      TileCursor nxt = cur;
+      const bool have_next = cursor_next<kSparse>(p, nxt, it1);
+      if (have_next) fetch_indices(nxt);  // in flight while this tile streams
+      for (int c = 0; c < kNumChunks; ++c) {
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_k_empty + 8 * kst, kph ^ 1u, ctl));
+        if (!ok) break;
+        const uint32_t dst = sK + kst * kKStageBytes;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = krow0 + 4 * i;
+          cp_async_16(dst + r * 128 + ((seg ^ (r & 7)) << 4), src[i] + c * (kChunkElems * 2));
+        }
+        cp_async_commit();
+        ++issued;
+        if (issued > static_cast<uint32_t>(kCopyLag)) {
+          cp_async_wait<kCopyLag>();
+          fence_proxy_async();
+          mbar_arrive(bar_k_full + 8 * ast);
+          if (++ast == static_cast<uint32_t>(p.stages)) ast = 0;
+          ++marked;
+        }
+        if (++kst == static_cast<uint32_t>(p.stages)) {
+          kst = 0;
+          kph ^= 1u;
+        }
+      }
+      cur = nxt;
+      have = have_next;
     }
-    if (!ok && lane == 0) {
-      // Let every copy this warp started land before shared memory is released.
-      for (int s = 0; s < p.stages; ++s)
-        if (k_armed & (1u << s)) wait_drain(bar_k_full + 8 * s, (k_par >> s) & 1u, 100000000);
-      for (int c = 0; c < kNumChunks; ++c)
-        if (q_armed & (1u << c)) wait_drain(bar_q_full + 8 * c, (q_par >> c) & 1u, 100000000);
+    // Land the last stages; mark them full only on the normal path.
+    cp_async_wait<0>();
+    fence_proxy_async();
+    if (ok) {
+      while (marked < issued) {
+        mbar_arrive(bar_k_full + 8 * ast);
+        if (++ast == static_cast<uint32_t>(p.stages)) ast = 0;
+        ++marked;
+      }
     }
-  } else if (warp == 1) {
+  } else if (warp == kQWarp) {
+    // ============================================================ q loader
+    if (lane == 0) {
+      uint32_t qit = 0, q_armed = 0, q_par = 0;
+      bool ok = true;
+      const uint32_t q_tx = static_cast<uint32_t>(p.q_box_rows) * 128u;
+      for (int it = it0; it < it1 && ok; ++it) {
+        const WorkItem w = p.items[it];
+        int tl;
+        if (item_tiles<kSparse>(p, w, tl) == 0) continue;
+        for (int c = 0; c < kNumChunks; ++c) {
+          ok = wait_bounded(bar_q_empty + 8 * c, (qit & 1u) ^ 1u, ctl);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar_q_full + 8 * c, q_tx);
+          tma_load_2d(sQ + c * q_chunk_bytes, &tmap_q, c * kChunkElems, w.q_tok * p.G, bar_q_full + 8 * c);
+          q_armed |= 1u << c;
+          q_par = (q_par & ~(1u << c)) | ((qit & 1u) << c);
+        }
+        ++qit;
+      }
+      if (!ok) {
+        // Let every copy this thread started land before shared memory is released.
+        for (int c = 0; c < kNumChunks; ++c)
+          if (q_armed & (1u << c)) wait_drain(bar_q_full + 8 * c, (q_par >> c) & 1u, 100000000);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
     // ============================================================ MMA issuer
     if (lane == 0) {
       uint32_t kst = 0, kph = 0, qit = 0, acc = 0;
@@ -416,11 +492,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(bar_teardown, 0, 200000000);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= kEpiWarp0) {
     // ============================================================ epilogue
-    const int wg = (warp - 4) >> 2;   // warpgroup 0 or 1
-    const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
-    const int et = quarter * 32 + lane;  // key slot inside the tile
+    const int wg = (warp - kEpiWarp0) >> 2;  // warpgroup 0 or 1
+    const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+    const int et = quarter * 32 + lane;      // key slot inside the tile
     float* L = ltab + wg * kAccCols;
     const int bar_id = 1 + wg;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
@@ -525,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(kAccBufs * kAccCols)
@@ -561,12 +637,12 @@ cudaError_t configure_fused(int smem_bytes) {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
-cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
-                         bool sparse, int grid, int smem_bytes, cudaStream_t stream) {
+cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int grid,
+                         int smem_bytes, cudaStream_t stream) {
   if (sparse)
-    smla_fused_kernel<true><<<grid, kThreads, smem_bytes, stream>>>(p, tmap_q, tmap_k);
+    smla_fused_kernel<true><<<grid, kThreads, smem_bytes, stream>>>(p, tmap_q);
   else
-    smla_fused_kernel<false><<<grid, kThreads, smem_bytes, stream>>>(p, tmap_q, tmap_k);
+    smla_fused_kernel<false><<<grid, kThreads, smem_bytes, stream>>>(p, tmap_q);
   return cudaGetLastError();
 }
 

@@ -243,19 +243,15 @@ extern "C" smla_status smla_l1norm_run_noalloc(const smla_l1norm_desc* desc, con
                         cudaMemcpyHostToDevice, cstream);
   if (e != cudaSuccess) return fail_cuda(e);
 
-  CUtensorMap tq, tk;
+  CUtensorMap tq;
   const int q_box = s.R * s.G;
   if (!encode_rows(&tq, q, s.q_rows, q_box, desc->dtype)) return SMLA_ERR_CUDA;
-  if (s.k_rows > 0) {
-    if (!encode_rows(&tk, k, s.k_rows, s.sparse ? 1 : smla::kTileKeys, desc->dtype)) return SMLA_ERR_CUDA;
-  } else {
-    tk = tq;
-  }
   const int64_t mma_m = 128;
   const uint32_t ab = desc->dtype == SMLA_DTYPE_BF16 ? 1u : 0u;
   const uint32_t idesc = (1u << 4) | (ab << 7) | (ab << 10) | (static_cast<uint32_t>(s.n_mma >> 3) << 17) |
                          (static_cast<uint32_t>(mma_m >> 4) << 24);
   smla::KernelParams p{};
+  p.k = static_cast<const uint8_t*>(k);
   p.items = reinterpret_cast<const WorkItem*>(dbase + kStatusBytes + kOffsetsBytes);
   p.cta_begin = reinterpret_cast<const int32_t*>(dbase + kStatusBytes);
   p.status = reinterpret_cast<int32_t*>(dbase);
@@ -276,7 +272,7 @@ extern "C" smla_status smla_l1norm_run_noalloc(const smla_l1norm_desc* desc, con
   p.inv_g = 1.0f / static_cast<float>(s.G);
   p.timeout_ns = 2000LL * 1000000LL;
   e = smla::configure_fused(smem);
-  if (e == cudaSuccess) e = smla::launch_fused(p, tq, tk, s.sparse, ctas, smem, cstream);
+  if (e == cudaSuccess) e = smla::launch_fused(p, tq, s.sparse, ctas, smem, cstream);
   if (e != cudaSuccess) return fail_cuda(e);
   return SMLA_OK;
 }
