@@ -22,7 +22,7 @@ constexpr int kKStageBytes = kTileKeys * kChunkElems * 2;  // 16 KB
 constexpr int kAccBufs = 4;
 constexpr int kAccCols = 128;
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 512;  // 16 warps: 4 key producers, MMA, q loader, 2 spare, 2 epilogue warpgroups
+constexpr int kThreads = 256;  // 8 warps: MMA, 2 key producers, q loader, one epilogue warpgroup
 
 // Status word bits.
 constexpr int kFlagBadIndex = 1;
@@ -71,7 +71,7 @@ inline int smem_bytes_for(int n_mma, int stages) {
   const int ring = stages * kKStageBytes;
   const int bars = (2 * kNumChunks + 2 * kMaxStages + 2 * kAccBufs + 2) * 8;
   const int tables = 2 * kAccCols * 4;  // per-warpgroup lse table
-  return 1024 /* alignment slack */ + q_bytes + ring + bars + tables + 64;
+  return 1024 /* alignment slack */ + q_bytes + ring + bars + tables + 128;
 }
 
 // Launch the fused kernel (defined in smla_kernel.cu).

@@ -7,26 +7,26 @@
 //     out[i] = 0                                                   otherwise
 // with j_i = sparse_indices[i] (stage 1 gather) or j_i = i (dense form).
 //
-// How (one persistent CTA per SM, 512 threads, warp-specialised):
-//   warps 0-3   key producers.  Each 128-key tile is moved in 8 stages of
+// How (one persistent CTA per SM, 256 threads, warp-specialised):
+//   warps 1, 3  key producers.  Each 128-key tile is moved in 8 stages of
 //               64 head-dim columns (128 keys x 128 bytes = 16 KB).  Every
 //               thread copies 16-byte pieces with cp.async straight into the
 //               128-byte-swizzle position the MMA descriptor expects (a warp
 //               instruction covers 4 whole 128-byte key rows), so any key
 //               order costs the same as a contiguous tile.  The key indices
 //               of the next tile are fetched while the current tile streams.
-//   warp 4      MMA issuer.  tcgen05.mma kind::f16, M = 128 keys (A = key
+//   warp 0      MMA issuer.  tcgen05.mma kind::f16, M = 128 keys (A = key
 //               stage), N = G heads padded to 16 (B = q chunk), K = 512 in
 //               32 steps of 16, fp32 accumulation in one of 4 TMEM buffers.
-//   warp 5      q loader.  TMA loads each token's q block (G heads x 512) as
+//   warp 2      q loader.  TMA loads each token's q block (G heads x 512) as
 //               8 chunks of 64 columns (SWIZZLE_128B); chunk c of the next
 //               token loads as soon as the last MMA of the current token has
-//               read chunk c.
-//   warps 8-15  two epilogue warpgroups taking alternate tiles.  Thread t
-//               owns TMEM lane t, i.e. key slot t of the tile, reads its G
-//               accumulator columns, and sums exp2(s*scale*log2e - lse*log2e)
-//               over the heads in registers: the head reduction needs no
-//               shuffles and the fp32 stores are coalesced across the warp.
+//               read chunk c, and the next tokens' blocks are prefetched to L2.
+//   warps 4-7   epilogue warpgroup.  Thread t owns TMEM lane t, i.e. key
+//               slot t of the tile, reads its G accumulator columns, and sums
+//               exp2(s*scale*log2e - lse*log2e) over the heads in registers:
+//               the head reduction needs no shuffles and the fp32 stores are
+//               coalesced across the warp.
 // The article's kernel splits the G heads of one token across cores and
 // merges them with atomic adds; here one CTA owns a token's whole G x slots
 // block, so each output element is written once, in a fixed order.
@@ -56,6 +56,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking test of phase completion.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -126,6 +138,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// Bring a box of a tensor into L2 ahead of its load (no shared memory used).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -171,6 +188,20 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The same MMA with the descriptors given as (low, high) 32-bit halves and a
+// constant accumulate flag: the issuing thread's per-MMA work is two moves.
+template <bool kAccumulate>
+__device__ __forceinline__ void umma_f16_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                              uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.u32 p, %6, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(kAccumulate ? 1 : 0)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -225,13 +256,19 @@ __device__ __forceinline__ bool wg_all(int id, bool v) {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Roles.
-constexpr int kProducerWarps = 4;   // warps 0-3
-constexpr int kMmaWarp = 4;
-constexpr int kQWarp = 5;
-constexpr int kEpiWarp0 = 8;        // warps 8-15
-// A producer thread keeps this many of its stages in flight before it waits
-// for the oldest one and marks it full (must stay below the ring depth).
+// Warps are spread over the four SM sub-partitions (warp % 4) so that the
+// single MMA-issuing thread shares its sub-partition with as little else as
+// possible: its issue rate is bound by its own instruction latency.
+constexpr int kMmaWarp = 0;         // sub-partition 0, with one epilogue warp
+constexpr int kQWarp = 2;
+constexpr int kProducerWarps = 2;   // warps 1 and 3
+constexpr int kKeysPerLane = kTileKeys / (kProducerWarps * 4);   // 16
+constexpr int kEpiWarp0 = 4;        // warps 4-7: one warpgroup
+constexpr int kEpiGroups = (kThreads / 32 - kEpiWarp0) / 4;
+// A producer warp keeps this many of its stages in flight before it waits
+// for the oldest and marks it full (below the ring depth).
 constexpr int kCopyLag = 3;
+__device__ __forceinline__ int producer_index(int warp) { return warp == 1 ? 0 : (warp == 3 ? 1 : -1); }
 
 // Key tiles an item needs, and (sparse form) the clamped topk_length.
 template <bool kSparse>
@@ -304,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_q_empty + 8 * c, 1);
     }
     for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(bar_k_full + 8 * s, kProducerWarps * 32);
+      mbar_init(bar_k_full + 8 * s, kProducerWarps);
       mbar_init(bar_k_empty + 8 * s, 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
@@ -339,22 +376,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int it0 = p.cta_begin[blockIdx.x];
   const int it1 = p.cta_begin[blockIdx.x + 1];
 
-  if (warp < kProducerWarps) {
+  const int pw = producer_index(warp);
+  if (pw >= 0) {
     // ============================================================ key producers
-    // Thread (warp pw, lane l) copies 16-byte segment (l & 7) of key rows
-    // pw*32 + (l >> 3) + 4*i, i = 0..7, of every stage.
+    // Producer warp pw, lane l copies 16-byte segment (l & 7) of key rows
+    // pw*64 + (l >> 3) + 4*i, i = 0..15, of every stage (4 whole 128-byte
+    // rows per warp instruction).  Stage n uses ring slot n % stages.  After
+    // issuing a stage the warp waits for its stage issued kCopyLag earlier,
+    // fences its (completed) writes for the async proxy and marks it full.
     const int seg = lane & 7;
-    const int krow0 = warp * 32 + (lane >> 3);
-    uint32_t kst = 0, kph = 0;   // ring slot being filled, its phase
-    uint32_t ast = 0;            // ring slot to mark full next
+    const int krow0 = pw * (kTileKeys / kProducerWarps) + (lane >> 3);
+    const uint32_t S = static_cast<uint32_t>(p.stages);
+    uint32_t kst = 0, kph = 0;   // slot being filled, its phase
+    uint32_t ast = 0;            // next slot to mark full
     uint32_t issued = 0, marked = 0;
     bool ok = true;
+    auto mark_one = [&]() {
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_k_full + 8 * ast);
+      ast = (ast + 1 == S) ? 0u : ast + 1;
+      ++marked;
+    };
     TileCursor cur{it0 - 1, 0, 0, 0, WorkItem{}};
     bool have = cursor_next<kSparse>(p, cur, it1);
-    int jn[8];
+    int jn[kKeysPerLane];
     auto fetch_indices = [&](const TileCursor& c) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < kKeysPerLane; ++i) {
         const int slot = c.t * kTileKeys + krow0 + 4 * i;
         if (kSparse) {
           jn[i] = slot < c.tl ? __ldg(p.idx + static_cast<int64_t>(c.w.q_tok) * p.topk + slot) : -1;
@@ -366,10 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (have) fetch_indices(cur);
     while (have && ok) {
       // source rows of this tile (invalid slots read key 0 of the sequence)
-      const uint8_t* src[8];
+      const uint8_t* src[kKeysPerLane];
       bool bad = false;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < kKeysPerLane; ++i) {
         const int j = jn[i];
         const bool in = (j >= 0) && (j < cur.w.Sk);
         if (kSparse) bad |= (krow0 + 4 * i + cur.t * kTileKeys < cur.tl) && !in && (j != -1);
@@ -384,22 +433,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const uint32_t dst = sK + kst * kKStageBytes;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kKeysPerLane; ++i) {
           const int r = krow0 + 4 * i;
           cp_async_16(dst + r * 128 + ((seg ^ (r & 7)) << 4), src[i] + c * (kChunkElems * 2));
         }
         cp_async_commit();
         ++issued;
+        kst = (kst + 1 == S) ? 0u : kst + 1;
+        kph ^= (kst == 0) ? 1u : 0u;
         if (issued > static_cast<uint32_t>(kCopyLag)) {
           cp_async_wait<kCopyLag>();
-          fence_proxy_async();
-          mbar_arrive(bar_k_full + 8 * ast);
-          if (++ast == static_cast<uint32_t>(p.stages)) ast = 0;
-          ++marked;
-        }
-        if (++kst == static_cast<uint32_t>(p.stages)) {
-          kst = 0;
-          kph ^= 1u;
+          mark_one();
         }
       }
       cur = nxt;
@@ -407,13 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Land the last stages; mark them full only on the normal path.
     cp_async_wait<0>();
-    fence_proxy_async();
     if (ok) {
-      while (marked < issued) {
-        mbar_arrive(bar_k_full + 8 * ast);
-        if (++ast == static_cast<uint32_t>(p.stages)) ast = 0;
-        ++marked;
-      }
+      while (marked < issued) mark_one();
     }
   } else if (warp == kQWarp) {
     // ============================================================ q loader
@@ -421,10 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t qit = 0, q_armed = 0, q_par = 0;
       bool ok = true;
       const uint32_t q_tx = static_cast<uint32_t>(p.q_box_rows) * 128u;
+      int pf = it0;  // next item whose q block is prefetched into L2
       for (int it = it0; it < it1 && ok; ++it) {
         const WorkItem w = p.items[it];
         int tl;
         if (item_tiles<kSparse>(p, w, tl) == 0) continue;
+        // keep the q blocks of the next two items on their way into L2
+        for (; pf < it1 && pf <= it + 2; ++pf)
+          for (int c = 0; c < kNumChunks; ++c)
+            tma_prefetch_l2_2d(&tmap_q, c * kChunkElems, p.items[pf].q_tok * p.G);
         for (int c = 0; c < kNumChunks; ++c) {
           ok = wait_bounded(bar_q_empty + 8 * c, (qit & 1u) ^ 1u, ctl);
           if (!ok) break;
@@ -444,7 +488,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ============================================================ MMA issuer
+    // One thread issues every MMA.  A single thread has no other work to hide
+    // its own instruction latency behind, so the loop is kept minimal: the
+    // descriptors differ only in their low word (start address), the 8
+    // chunks of a tile are unrolled, and the accumulate flag is a constant.
     if (lane == 0) {
+      const uint64_t a0 = sdesc_k_major_sw128(sK);
+      const uint64_t b0 = sdesc_k_major_sw128(sQ);
+      const uint32_t a_hi = static_cast<uint32_t>(a0 >> 32), b_hi = static_cast<uint32_t>(b0 >> 32);
+      const uint32_t a_lo0 = static_cast<uint32_t>(a0), b_lo0 = static_cast<uint32_t>(b0);
+      const uint32_t b_step = static_cast<uint32_t>(q_chunk_bytes) >> 4;
+      const uint32_t idesc = static_cast<uint32_t>(p.idesc);
+      const uint32_t S = static_cast<uint32_t>(p.stages);
       uint32_t kst = 0, kph = 0, qit = 0, acc = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
@@ -452,35 +507,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tl;
         const int nt = item_tiles<kSparse>(p, w, tl);
         if (nt == 0) continue;
+        for (int c = 0; c < kNumChunks && ok; ++c) ok = wait_bounded(bar_q_full + 8 * c, qit & 1u, ctl);
         for (int t = 0; t < nt && ok; ++t, ++acc) {
           const uint32_t buf = acc & (kAccBufs - 1);
-          const uint32_t use = acc / kAccBufs;
-          ok = wait_bounded(bar_acc_empty + 8 * buf, (use & 1u) ^ 1u, ctl);
+          ok = wait_bounded(bar_acc_empty + 8 * buf, ((acc / kAccBufs) & 1u) ^ 1u, ctl);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * kAccCols;
+          const bool last = (t == nt - 1);
+#pragma unroll
           for (int c = 0; c < kNumChunks; ++c) {
-            if (t == 0) {
-              ok = wait_bounded(bar_q_full + 8 * c, qit & 1u, ctl);
-              if (!ok) break;
-            }
             ok = wait_bounded(bar_k_full + 8 * kst, kph, ctl);
             if (!ok) break;
             tc_fence_after();
-            const uint64_t a_desc = sdesc_k_major_sw128(sK + kst * kKStageBytes);
-            const uint64_t b_desc = sdesc_k_major_sw128(sQ + c * q_chunk_bytes);
-#pragma unroll
-            for (int k = 0; k < kChunkElems / 16; ++k) {
-              // advance 16 elements (32 bytes) along K inside the swizzled row
-              umma_f16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, static_cast<uint32_t>(p.idesc),
-                       (c | k) != 0 ? 1u : 0u);
-            }
+            const uint32_t a_lo = a_lo0 + kst * (kKStageBytes >> 4);
+            const uint32_t b_lo = b_lo0 + c * b_step;
+            // 4 K-steps of 16 elements (32 bytes) inside the swizzled rows
+            if (c == 0)
+              umma_f16_lohi<false>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
+            else
+              umma_f16_lohi<true>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
+            umma_f16_lohi<true>(d_tmem, a_lo + 2, a_hi, b_lo + 2, b_hi, idesc);
+            umma_f16_lohi<true>(d_tmem, a_lo + 4, a_hi, b_lo + 4, b_hi, idesc);
+            umma_f16_lohi<true>(d_tmem, a_lo + 6, a_hi, b_lo + 6, b_hi, idesc);
             umma_commit(bar_k_empty + 8 * kst);
-            if (t == nt - 1) umma_commit(bar_q_empty + 8 * c);
-            if (++kst == static_cast<uint32_t>(p.stages)) {
-              kst = 0;
-              kph ^= 1u;
-            }
+            if (last) umma_commit(bar_q_empty + 8 * c);
+            kst = (kst + 1 == S) ? 0u : kst + 1;
+            kph ^= (kst == 0) ? 1u : 0u;
           }
           if (!ok) break;
           umma_commit(bar_acc_full + 8 * buf);
@@ -494,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ============================================================ epilogue
-    const int wg = (warp - kEpiWarp0) >> 2;  // warpgroup 0 or 1
+    const int wg = (warp - kEpiWarp0) >> 2;  // epilogue warpgroup
     const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
     const int et = quarter * 32 + lane;      // key slot inside the tile
     float* L = ltab + wg * kAccCols;
@@ -509,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tl;
       const int nt = item_tiles<kSparse>(p, w, tl);
       for (int t = 0; t < nt; ++t, ++acc) {
-        if (static_cast<int>(acc & 1u) != wg) continue;
+        if (static_cast<int>(acc % kEpiGroups) != wg) continue;
         if (table_item != it) {
           // lse * log2(e) per accumulator column; +inf beyond the real heads
           // so that padded columns contribute exp2(-inf) = 0.
@@ -584,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // Slots past the last computed tile are zero.
-      if (((it - it0) & 1) == wg) {
+      if ((it - it0) % kEpiGroups == wg) {
         if (kSparse) {
           float* o = p.out + static_cast<int64_t>(w.q_tok) * p.topk;
           for (int s = nt * kTileKeys + et; s < p.topk; s += kTileKeys) o[s] = 0.f;
