@@ -18,11 +18,15 @@ constexpr int kTileKeys = 128;
 constexpr int kChunkElems = 64;
 constexpr int kNumChunks = kHeadDim / kChunkElems;  // 8
 constexpr int kKStageBytes = kTileKeys * kChunkElems * 2;  // 16 KB
-// TMEM accumulators: 4 buffers of 128 fp32 columns (all 512 columns).
-constexpr int kAccBufs = 4;
-constexpr int kAccCols = 128;
+// TMEM accumulators: 2 tile buffers of 256 fp32 columns (all 512 columns);
+// each buffer holds two partial sums of 128 columns (even / odd head-dim
+// chunks), issued by two MMA threads.
+constexpr int kAccBufs = 2;
+constexpr int kAccCols = 256;
+constexpr int kHalfCols = 128;
+constexpr int kMaxN = 128;  // largest MMA N (R*G padded to 16)
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 256;  // 8 warps: MMA, 2 key producers, q loader, one epilogue warpgroup
+constexpr int kThreads = 288;  // 9 warps: 2 MMA issuers, 2 key producers, one epilogue warpgroup, q loader
 
 // Status word bits.
 constexpr int kFlagBadIndex = 1;
@@ -70,7 +74,7 @@ inline int smem_bytes_for(int n_mma, int stages) {
   const int q_bytes = kNumChunks * n_mma * 128;
   const int ring = stages * kKStageBytes;
   const int bars = (2 * kNumChunks + 2 * kMaxStages + 2 * kAccBufs + 2) * 8;
-  const int tables = 2 * kAccCols * 4;  // per-warpgroup lse table
+  const int tables = kMaxN * 4;  // lse table of the epilogue warpgroup
   return 1024 /* alignment slack */ + q_bytes + ring + bars + tables + 128;
 }
 

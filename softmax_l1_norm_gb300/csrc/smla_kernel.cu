@@ -7,7 +7,7 @@
 //     out[i] = 0                                                   otherwise
 // with j_i = sparse_indices[i] (stage 1 gather) or j_i = i (dense form).
 //
-// How (one persistent CTA per SM, 256 threads, warp-specialised):
+// How (one persistent CTA per SM, 288 threads, warp-specialised):
 //   warps 1, 3  key producers.  Each 128-key tile is moved in 8 stages of
 //               64 head-dim columns (128 keys x 128 bytes = 16 KB).  Every
 //               thread copies 16-byte pieces with cp.async straight into the
@@ -15,15 +15,19 @@
 //               instruction covers 4 whole 128-byte key rows), so any key
 //               order costs the same as a contiguous tile.  The key indices
 //               of the next tile are fetched while the current tile streams.
-//   warp 0      MMA issuer.  tcgen05.mma kind::f16, M = 128 keys (A = key
+//   warps 0, 2  MMA issuers.  tcgen05.mma kind::f16, M = 128 keys (A = key
 //               stage), N = G heads padded to 16 (B = q chunk), K = 512 in
-//               32 steps of 16, fp32 accumulation in one of 4 TMEM buffers.
-//   warp 2      q loader.  TMA loads each token's q block (G heads x 512) as
+//               32 steps of 16, fp32 accumulation in TMEM.  One thread cannot
+//               issue M128xN128xK16 MMAs as fast as the tensor core runs them,
+//               so two threads on different sub-partitions split K: warp 0
+//               takes the even 64-column chunks, warp 2 the odd ones, each into
+//               its own half of the tile's 256-column TMEM buffer.
+//   warp 8      q loader.  TMA loads each token's q block (G heads x 512) as
 //               8 chunks of 64 columns (SWIZZLE_128B); chunk c of the next
 //               token loads as soon as the last MMA of the current token has
 //               read chunk c, and the next tokens' blocks are prefetched to L2.
 //   warps 4-7   epilogue warpgroup.  Thread t owns TMEM lane t, i.e. key
-//               slot t of the tile, reads its G accumulator columns, and sums
+//               slot t of the tile, adds its two partial accumulators, and sums
 //               exp2(s*scale*log2e - lse*log2e) over the heads in registers:
 //               the head reduction needs no shuffles and the fp32 stores are
 //               coalesced across the warp.
@@ -150,12 +154,13 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// Arrive on the barrier once every cp.async this thread has issued so far
+// has landed (the arrival counts against the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 // Make this thread's completed generic-proxy shared-memory writes visible to
 // the async proxy (the tensor cores read their operands through it).
@@ -259,15 +264,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Warps are spread over the four SM sub-partitions (warp % 4) so that the
 // single MMA-issuing thread shares its sub-partition with as little else as
 // possible: its issue rate is bound by its own instruction latency.
-constexpr int kMmaWarp = 0;         // sub-partition 0, with one epilogue warp
-constexpr int kQWarp = 2;
+constexpr int kMmaWarpA = 0;        // even head-dim chunks; sub-partition 0
+constexpr int kMmaWarpB = 2;        // odd head-dim chunks; sub-partition 2
+constexpr int kQWarp = 8;           // sleeps in barrier waits most of the time
 constexpr int kProducerWarps = 2;   // warps 1 and 3
 constexpr int kKeysPerLane = kTileKeys / (kProducerWarps * 4);   // 16
 constexpr int kEpiWarp0 = 4;        // warps 4-7: one warpgroup
-constexpr int kEpiGroups = (kThreads / 32 - kEpiWarp0) / 4;
-// A producer warp keeps this many of its stages in flight before it waits
-// for the oldest and marks it full (below the ring depth).
-constexpr int kCopyLag = 3;
+constexpr int kEpiGroups = 1;
 __device__ __forceinline__ int producer_index(int warp) { return warp == 1 ? 0 : (warp == 3 ? 1 : -1); }
 
 // Key tiles an item needs, and (sparse form) the clamped topk_length.
@@ -301,6 +304,77 @@ __device__ __forceinline__ bool cursor_next(const KernelParams& p, TileCursor& c
     c.t = 0;
   }
   return true;
+}
+
+struct MmaCtx {
+  uint32_t sK, sQ;
+  int q_chunk_bytes;
+  uint32_t bar_q_full, bar_q_empty, bar_k_full, bar_k_empty, bar_acc_full, bar_acc_empty;
+  uint32_t tmem_base;
+  int it0, it1;
+};
+
+// MMA issuer H (0 or 1) handles the head-dim chunks c with c % 2 == H of
+// every tile, accumulating into its own 128-column half of the tile's TMEM
+// buffer; the epilogue adds the two halves.  One thread issues every MMA of
+// its half.  A single thread has no other work to hide its own instruction
+// latency behind, so the loop is kept minimal: the descriptors differ only
+// in their low word (start address), the chunk loop is unrolled and the
+// accumulate flag is a constant.
+template <bool kSparse, int H>
+__device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m, const WaitCtl& ctl) {
+  const uint64_t a0 = sdesc_k_major_sw128(m.sK);
+  const uint64_t b0 = sdesc_k_major_sw128(m.sQ);
+  const uint32_t a_hi = static_cast<uint32_t>(a0 >> 32), b_hi = static_cast<uint32_t>(b0 >> 32);
+  const uint32_t a_lo0 = static_cast<uint32_t>(a0), b_lo0 = static_cast<uint32_t>(b0);
+  const uint32_t b_step = static_cast<uint32_t>(m.q_chunk_bytes) >> 4;
+  const uint32_t idesc = static_cast<uint32_t>(p.idesc);
+  const uint32_t S = static_cast<uint32_t>(p.stages);
+  uint32_t kst = 0, kph = 0, qit = 0, acc = 0;
+  bool ok = true;
+  for (int it = m.it0; it < m.it1 && ok; ++it) {
+    const WorkItem w = p.items[it];
+    int tl;
+    const int nt = item_tiles<kSparse>(p, w, tl);
+    if (nt == 0) continue;
+    for (int c = H; c < kNumChunks && ok; c += 2) ok = wait_bounded(m.bar_q_full + 8 * c, qit & 1u, ctl);
+    for (int t = 0; t < nt && ok; ++t, ++acc) {
+      const uint32_t buf = acc & (kAccBufs - 1);
+      ok = wait_bounded(m.bar_acc_empty + 8 * buf, ((acc / kAccBufs) & 1u) ^ 1u, ctl);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = m.tmem_base + buf * kAccCols + H * kHalfCols;
+      const bool last = (t == nt - 1);
+#pragma unroll
+      for (int c = 0; c < kNumChunks; ++c) {
+        if ((c & 1) == H) {
+          ok = wait_bounded(m.bar_k_full + 8 * kst, kph, ctl);
+          if (!ok) break;
+          // the producers' cp.async writes (generic proxy), acquired through
+          // the barrier, become visible to the tensor cores (async proxy)
+          fence_proxy_async();
+          tc_fence_after();
+          const uint32_t a_lo = a_lo0 + kst * (kKStageBytes >> 4);
+          const uint32_t b_lo = b_lo0 + c * b_step;
+          // 4 K-steps of 16 elements (32 bytes) inside the swizzled rows
+          if (c == H)
+            umma_f16_lohi<false>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
+          else
+            umma_f16_lohi<true>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
+          umma_f16_lohi<true>(d_tmem, a_lo + 2, a_hi, b_lo + 2, b_hi, idesc);
+          umma_f16_lohi<true>(d_tmem, a_lo + 4, a_hi, b_lo + 4, b_hi, idesc);
+          umma_f16_lohi<true>(d_tmem, a_lo + 6, a_hi, b_lo + 6, b_hi, idesc);
+          umma_commit(m.bar_k_empty + 8 * kst);
+          if (last) umma_commit(m.bar_q_empty + 8 * c);
+        }
+        kst = (kst + 1 == S) ? 0u : kst + 1;
+        kph ^= (kst == 0) ? 1u : 0u;
+      }
+      if (!ok) break;
+      umma_commit(m.bar_acc_full + 8 * buf);
+    }
+    ++qit;
+  }
 }
 
 }  // namespace
@@ -341,14 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_q_empty + 8 * c, 1);
     }
     for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(bar_k_full + 8 * s, kProducerWarps);
+      mbar_init(bar_k_full + 8 * s, kProducerWarps * 32);
       mbar_init(bar_k_empty + 8 * s, 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
-      mbar_init(bar_acc_full + 8 * b, 1);
+      mbar_init(bar_acc_full + 8 * b, 2);   // one commit per MMA issuer
       mbar_init(bar_acc_empty + 8 * b, 128);
     }
-    mbar_init(bar_teardown, 1);
+    mbar_init(bar_teardown, 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -360,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i < n16; i += blockDim.x) q4[i] = make_uint4(0, 0, 0, 0);
   }
   fence_proxy_async();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarpA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(kAccBufs * kAccCols)
@@ -381,23 +455,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================================================ key producers
     // Producer warp pw, lane l copies 16-byte segment (l & 7) of key rows
     // pw*64 + (l >> 3) + 4*i, i = 0..15, of every stage (4 whole 128-byte
-    // rows per warp instruction).  Stage n uses ring slot n % stages.  After
-    // issuing a stage the warp waits for its stage issued kCopyLag earlier,
-    // fences its (completed) writes for the async proxy and marks it full.
+    // rows per warp instruction).  Stage n uses ring slot n % stages.  Each
+    // lane's copies arrive on the slot's full barrier by themselves when
+    // they land (cp.async.mbarrier.arrive.noinc), so a producer only waits
+    // for free slots and every slot of the ring can be in flight.  The
+    // generic-to-async proxy fence the tensor cores need is executed by the
+    // MMA thread after it acquires the full barrier: in a producer it would
+    // also wait for the copies still in flight.
     const int seg = lane & 7;
     const int krow0 = pw * (kTileKeys / kProducerWarps) + (lane >> 3);
     const uint32_t S = static_cast<uint32_t>(p.stages);
     uint32_t kst = 0, kph = 0;   // slot being filled, its phase
-    uint32_t ast = 0;            // next slot to mark full
-    uint32_t issued = 0, marked = 0;
     bool ok = true;
-    auto mark_one = [&]() {
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_k_full + 8 * ast);
-      ast = (ast + 1 == S) ? 0u : ast + 1;
-      ++marked;
-    };
     TileCursor cur{it0 - 1, 0, 0, 0, WorkItem{}};
     bool have = cursor_next<kSparse>(p, cur, it1);
     int jn[kKeysPerLane];
@@ -437,23 +506,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = krow0 + 4 * i;
           cp_async_16(dst + r * 128 + ((seg ^ (r & 7)) << 4), src[i] + c * (kChunkElems * 2));
         }
-        cp_async_commit();
-        ++issued;
+        cp_async_arrive_noinc(bar_k_full + 8 * kst);
         kst = (kst + 1 == S) ? 0u : kst + 1;
         kph ^= (kst == 0) ? 1u : 0u;
-        if (issued > static_cast<uint32_t>(kCopyLag)) {
-          cp_async_wait<kCopyLag>();
-          mark_one();
-        }
       }
       cur = nxt;
       have = have_next;
     }
-    // Land the last stages; mark them full only on the normal path.
-    cp_async_wait<0>();
-    if (ok) {
-      while (marked < issued) mark_one();
-    }
+    // Copies still in flight land before shared memory is released.
+    cp_async_wait_all();
   } else if (warp == kQWarp) {
     // ============================================================ q loader
     if (lane == 0) {
@@ -486,60 +547,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ============================================================ MMA issuer
-    // One thread issues every MMA.  A single thread has no other work to hide
-    // its own instruction latency behind, so the loop is kept minimal: the
-    // descriptors differ only in their low word (start address), the 8
-    // chunks of a tile are unrolled, and the accumulate flag is a constant.
+  } else if (warp == kMmaWarpA || warp == kMmaWarpB) {
+    // ============================================================ MMA issuers
     if (lane == 0) {
-      const uint64_t a0 = sdesc_k_major_sw128(sK);
-      const uint64_t b0 = sdesc_k_major_sw128(sQ);
-      const uint32_t a_hi = static_cast<uint32_t>(a0 >> 32), b_hi = static_cast<uint32_t>(b0 >> 32);
-      const uint32_t a_lo0 = static_cast<uint32_t>(a0), b_lo0 = static_cast<uint32_t>(b0);
-      const uint32_t b_step = static_cast<uint32_t>(q_chunk_bytes) >> 4;
-      const uint32_t idesc = static_cast<uint32_t>(p.idesc);
-      const uint32_t S = static_cast<uint32_t>(p.stages);
-      uint32_t kst = 0, kph = 0, qit = 0, acc = 0;
-      bool ok = true;
-      for (int it = it0; it < it1 && ok; ++it) {
-        const WorkItem w = p.items[it];
-        int tl;
-        const int nt = item_tiles<kSparse>(p, w, tl);
-        if (nt == 0) continue;
-        for (int c = 0; c < kNumChunks && ok; ++c) ok = wait_bounded(bar_q_full + 8 * c, qit & 1u, ctl);
-        for (int t = 0; t < nt && ok; ++t, ++acc) {
-          const uint32_t buf = acc & (kAccBufs - 1);
-          ok = wait_bounded(bar_acc_empty + 8 * buf, ((acc / kAccBufs) & 1u) ^ 1u, ctl);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + buf * kAccCols;
-          const bool last = (t == nt - 1);
-#pragma unroll
-          for (int c = 0; c < kNumChunks; ++c) {
-            ok = wait_bounded(bar_k_full + 8 * kst, kph, ctl);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t a_lo = a_lo0 + kst * (kKStageBytes >> 4);
-            const uint32_t b_lo = b_lo0 + c * b_step;
-            // 4 K-steps of 16 elements (32 bytes) inside the swizzled rows
-            if (c == 0)
-              umma_f16_lohi<false>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
-            else
-              umma_f16_lohi<true>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
-            umma_f16_lohi<true>(d_tmem, a_lo + 2, a_hi, b_lo + 2, b_hi, idesc);
-            umma_f16_lohi<true>(d_tmem, a_lo + 4, a_hi, b_lo + 4, b_hi, idesc);
-            umma_f16_lohi<true>(d_tmem, a_lo + 6, a_hi, b_lo + 6, b_hi, idesc);
-            umma_commit(bar_k_empty + 8 * kst);
-            if (last) umma_commit(bar_q_empty + 8 * c);
-            kst = (kst + 1 == S) ? 0u : kst + 1;
-            kph ^= (kst == 0) ? 1u : 0u;
-          }
-          if (!ok) break;
-          umma_commit(bar_acc_full + 8 * buf);
-        }
-        ++qit;
-      }
+      const MmaCtx m{sK, sQ, q_chunk_bytes, bar_q_full, bar_q_empty, bar_k_full, bar_k_empty,
+                     bar_acc_full, bar_acc_empty, tmem_base, it0, it1};
+      if (warp == kMmaWarpA)
+        mma_issue<kSparse, 0>(p, m, ctl);
+      else
+        mma_issue<kSparse, 1>(p, m, ctl);
       // All MMAs this thread issued must be complete before TMEM is released.
       umma_commit(bar_teardown);
       wait_drain(bar_teardown, 0, 200000000);
@@ -550,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = (warp - kEpiWarp0) >> 2;  // epilogue warpgroup
     const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
     const int et = quarter * 32 + lane;      // key slot inside the tile
-    float* L = ltab + wg * kAccCols;
+    float* L = ltab + wg * kMaxN;
     const int bar_id = 1 + wg;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t acc = 0;
@@ -596,12 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kSparse) {
           float s0 = 0.f, s1 = 0.f;
           for (int c0 = 0; c0 < p.n_mma; c0 += 16) {
-            float f[16];
+            float f[16], g[16];
             tmem_ld16(taddr + c0, f);
+            tmem_ld16(taddr + kHalfCols + c0, g);
 #pragma unroll
             for (int k = 0; k < 16; k += 2) {
-              s0 += fast_exp2(fmaf(f[k], c2, -L[c0 + k]));
-              s1 += fast_exp2(fmaf(f[k + 1], c2, -L[c0 + k + 1]));
+              s0 += fast_exp2(fmaf(f[k] + g[k], c2, -L[c0 + k]));
+              s1 += fast_exp2(fmaf(f[k + 1] + g[k + 1], c2, -L[c0 + k + 1]));
             }
           }
           tc_fence_before();
@@ -614,11 +631,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           float s = 0.f;
           int g_in = 0, r = 0;
           for (int c0 = 0; c0 < p.n_mma; c0 += 16) {
-            float f[16];
+            float f[16], g[16];
             tmem_ld16(taddr + c0, f);
+            tmem_ld16(taddr + kHalfCols + c0, g);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              s += fast_exp2(fmaf(f[k], c2, -L[c0 + k]));
+              s += fast_exp2(fmaf(f[k] + g[k], c2, -L[c0 + k]));
               if (++g_in == p.G) {
                 if (r < w.nrows && j < p.width) {
                   const bool v = (j < w.Sk) &&
@@ -654,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarpA) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(kAccBufs * kAccCols)
