@@ -26,7 +26,7 @@ constexpr int kAccCols = 256;
 constexpr int kHalfCols = 128;
 constexpr int kMaxN = 128;  // largest MMA N (R*G padded to 16)
 constexpr int kMaxStages = 8;
-constexpr int kThreads = 288;  // 9 warps: 2 MMA issuers, 2 key producers, one epilogue warpgroup, q loader
+constexpr int kThreads = 384;  // 12 warps: 2 MMA issuers, 4 key producers, one epilogue warpgroup, q loader, 1 spare
 
 // Status word bits.
 constexpr int kFlagBadIndex = 1;

@@ -7,8 +7,8 @@
 //     out[i] = 0                                                   otherwise
 // with j_i = sparse_indices[i] (stage 1 gather) or j_i = i (dense form).
 //
-// How (one persistent CTA per SM, 288 threads, warp-specialised):
-//   warps 1, 3  key producers.  Each 128-key tile is moved in 8 stages of
+// How (one persistent CTA per SM, 384 threads, warp-specialised):
+//   warps 1, 3, 9, 11  key producers.  Each 128-key tile is moved in 8 stages of
 //               64 head-dim columns (128 keys x 128 bytes = 16 KB).  Every
 //               thread copies 16-byte pieces with cp.async straight into the
 //               128-byte-swizzle position the MMA descriptor expects (a warp
@@ -267,11 +267,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMmaWarpA = 0;        // even head-dim chunks; sub-partition 0
 constexpr int kMmaWarpB = 2;        // odd head-dim chunks; sub-partition 2
 constexpr int kQWarp = 8;           // sleeps in barrier waits most of the time
-constexpr int kProducerWarps = 2;   // warps 1 and 3
-constexpr int kKeysPerLane = kTileKeys / (kProducerWarps * 4);   // 16
+constexpr int kProducerWarps = 4;   // warps 1, 3, 9, 11 (sub-partitions 1 and 3)
+constexpr int kKeysPerLane = kTileKeys / (kProducerWarps * 4);   // 8
 constexpr int kEpiWarp0 = 4;        // warps 4-7: one warpgroup
 constexpr int kEpiGroups = 1;
-__device__ __forceinline__ int producer_index(int warp) { return warp == 1 ? 0 : (warp == 3 ? 1 : -1); }
+__device__ __forceinline__ int producer_index(int warp) {
+  switch (warp) {
+    case 1: return 0;
+    case 3: return 1;
+    case 9: return 2;
+    case 11: return 3;
+    default: return -1;
+  }
+}
 
 // Key tiles an item needs, and (sparse form) the clamped topk_length.
 template <bool kSparse>
@@ -345,30 +353,43 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
       tc_fence_after();
       const uint32_t d_tmem = m.tmem_base + buf * kAccCols + H * kHalfCols;
       const bool last = (t == nt - 1);
+      // ring slot and phase of each of the tile's 8 stages
+      uint32_t sl[kNumChunks], ph[kNumChunks];
 #pragma unroll
       for (int c = 0; c < kNumChunks; ++c) {
-        if ((c & 1) == H) {
-          ok = wait_bounded(m.bar_k_full + 8 * kst, kph, ctl);
-          if (!ok) break;
-          // the producers' cp.async writes (generic proxy), acquired through
-          // the barrier, become visible to the tensor cores (async proxy)
-          fence_proxy_async();
-          tc_fence_after();
-          const uint32_t a_lo = a_lo0 + kst * (kKStageBytes >> 4);
-          const uint32_t b_lo = b_lo0 + c * b_step;
-          // 4 K-steps of 16 elements (32 bytes) inside the swizzled rows
-          if (c == H)
-            umma_f16_lohi<false>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
-          else
-            umma_f16_lohi<true>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
-          umma_f16_lohi<true>(d_tmem, a_lo + 2, a_hi, b_lo + 2, b_hi, idesc);
-          umma_f16_lohi<true>(d_tmem, a_lo + 4, a_hi, b_lo + 4, b_hi, idesc);
-          umma_f16_lohi<true>(d_tmem, a_lo + 6, a_hi, b_lo + 6, b_hi, idesc);
-          umma_commit(m.bar_k_empty + 8 * kst);
-          if (last) umma_commit(m.bar_q_empty + 8 * c);
-        }
+        sl[c] = kst;
+        ph[c] = kph;
         kst = (kst + 1 == S) ? 0u : kst + 1;
         kph ^= (kst == 0) ? 1u : 0u;
+      }
+      // The barrier test for the next stage is issued before the current
+      // stage's MMAs so that its latency overlaps them; only a stage that is
+      // not ready yet costs a blocking wait.
+      bool ready = mbar_test_wait(m.bar_k_full + 8 * sl[H], ph[H]);
+#pragma unroll
+      for (int c = H; c < kNumChunks; c += 2) {
+        if (!ready) {
+          ok = wait_bounded(m.bar_k_full + 8 * sl[c], ph[c], ctl);
+          if (!ok) break;
+        }
+        const bool ready_next = (c + 2 < kNumChunks) ? mbar_test_wait(m.bar_k_full + 8 * sl[c + 2], ph[c + 2]) : false;
+        // the producers' cp.async writes (generic proxy), acquired through
+        // the barrier, become visible to the tensor cores (async proxy)
+        fence_proxy_async();
+        tc_fence_after();
+        const uint32_t a_lo = a_lo0 + sl[c] * (kKStageBytes >> 4);
+        const uint32_t b_lo = b_lo0 + c * b_step;
+        // 4 K-steps of 16 elements (32 bytes) inside the swizzled rows
+        if (c == H)
+          umma_f16_lohi<false>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
+        else
+          umma_f16_lohi<true>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
+        umma_f16_lohi<true>(d_tmem, a_lo + 2, a_hi, b_lo + 2, b_hi, idesc);
+        umma_f16_lohi<true>(d_tmem, a_lo + 4, a_hi, b_lo + 4, b_hi, idesc);
+        umma_f16_lohi<true>(d_tmem, a_lo + 6, a_hi, b_lo + 6, b_hi, idesc);
+        umma_commit(m.bar_k_empty + 8 * sl[c]);
+        if (last) umma_commit(m.bar_q_empty + 8 * c);
+        ready = ready_next;
       }
       if (!ok) break;
       umma_commit(m.bar_acc_full + 8 * buf);
@@ -454,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (pw >= 0) {
     // ============================================================ key producers
     // Producer warp pw, lane l copies 16-byte segment (l & 7) of key rows
-    // pw*64 + (l >> 3) + 4*i, i = 0..15, of every stage (4 whole 128-byte
+    // pw*32 + (l >> 3) + 4*i, i = 0..7, of every stage (4 whole 128-byte
     // rows per warp instruction).  Stage n uses ring slot n % stages.  Each
     // lane's copies arrive on the slot's full barrier by themselves when
     // they land (cp.async.mbarrier.arrive.noinc), so a producer only waits
@@ -561,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(bar_teardown, 0, 200000000);
     }
     __syncwarp();
-  } else if (warp >= kEpiWarp0) {
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4 * kEpiGroups) {
     // ============================================================ epilogue
     const int wg = (warp - kEpiWarp0) >> 2;  // epilogue warpgroup
     const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
