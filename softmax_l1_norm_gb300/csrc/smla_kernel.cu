@@ -340,12 +340,14 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
   const uint32_t S = static_cast<uint32_t>(p.stages);
   uint32_t kst = 0, kph = 0, qit = 0, acc = 0;
   bool ok = true;
+  WorkItem w_next = m.it0 < m.it1 ? p.items[m.it0] : WorkItem{};
   for (int it = m.it0; it < m.it1 && ok; ++it) {
-    const WorkItem w = p.items[it];
+    const WorkItem w = w_next;
+    if (it + 1 < m.it1) w_next = p.items[it + 1];  // in flight while this item runs
     int tl;
     const int nt = item_tiles<kSparse>(p, w, tl);
     if (nt == 0) continue;
-    for (int c = H; c < kNumChunks && ok; c += 2) ok = wait_bounded(m.bar_q_full + 8 * c, qit & 1u, ctl);
+    const uint32_t qpar = qit & 1u;
     for (int t = 0; t < nt && ok; ++t, ++acc) {
       const uint32_t buf = acc & (kAccBufs - 1);
       ok = wait_bounded(m.bar_acc_empty + 8 * buf, ((acc / kAccBufs) & 1u) ^ 1u, ctl);
@@ -370,6 +372,11 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
       for (int c = H; c < kNumChunks; c += 2) {
         if (!ready) {
           ok = wait_bounded(m.bar_k_full + 8 * sl[c], ph[c], ctl);
+          if (!ok) break;
+        }
+        // q chunk c of a new token was freed about 8 stages ago
+        if (t == 0) {
+          ok = wait_bounded(m.bar_q_full + 8 * c, qpar, ctl);
           if (!ok) break;
         }
         const bool ready_next = (c + 2 < kNumChunks) ? mbar_test_wait(m.bar_k_full + 8 * sl[c + 2], ph[c + 2]) : false;
