@@ -47,6 +47,12 @@ its reason in the design notes of this repository):
   R9  stage 3 divides by G in fp64 (the GPU multiplies by fp32 1/G; the two
       agree within the stated tolerance and exactly for power-of-two G).
   R10 the result is rounded once, to nearest float32.
+  R11 seqused_q / seqused_k (parameter table: the number of q / k tokens of
+      each batch entry that actually take part in the computation): the
+      sequence's effective lengths become Sq' = min(Sq, seqused_q[b]) and
+      Sk' = min(Sk, seqused_k[b]); query rows r >= Sq' are all 0, keys
+      j >= Sk' are masked, and mask_mode 3 uses the effective lengths
+      (j <= r + Sk' - Sq').
 
 Inputs are the rounded half-precision tensors as raw 16-bit patterns plus a
 dtype tag; every product and sum is carried out in float64.
@@ -188,8 +194,19 @@ def _width(layout, k_shape, sparse_indices, max_seqlen_k):
     return int(max_seqlen_k) if layout == "TND" else int(k_shape[1])
 
 
-def _row_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length, width, mask_mode):
-    b, r, Sq, k0, Sk = geo[t]
+def _effective(geo_t, seqused_q, seqused_k):
+    """(b, r, Sq', k0, Sk') with the participating lengths (reading R11)."""
+    b, r, Sq, k0, Sk = geo_t
+    if seqused_q is not None:
+        Sq = max(0, min(Sq, int(np.asarray(seqused_q).reshape(-1)[b])))
+    if seqused_k is not None:
+        Sk = max(0, min(Sk, int(np.asarray(seqused_k).reshape(-1)[b])))
+    return b, r, Sq, k0, Sk
+
+
+def _row_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length, width, mask_mode,
+               seqused_q=None, seqused_k=None):
+    b, r, Sq, k0, Sk = _effective(geo[t], seqused_q, seqused_k)
     idx_row = None
     tl = None
     if sparse_indices is not None:
@@ -198,8 +215,13 @@ def _row_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length, width, mask_m
             tl = int(np.asarray(topk_length).reshape(-1)[t])
     j = slot_key_positions(idx_row, width)
     valid = slot_valid(j, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=tl)
+    if r >= Sq:                                # a query row that does not take part
+        valid = np.zeros_like(valid)
     rows = np.where(valid, k0 + j, 0)          # key rows (any row for invalid slots)
-    sel_k = decode_half(kv[rows], dtype)       # stage 1 gather
+    if kv.shape[0] == 0:                       # no key row at all: every slot is invalid
+        sel_k = np.zeros((len(rows), kv.shape[1]))
+    else:
+        sel_k = decode_half(kv[rows], dtype)   # stage 1 gather
     q_row = decode_half(qv[t], dtype)
     return q_row, sel_k, valid
 
@@ -207,7 +229,8 @@ def _row_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length, width, mask_m
 def softmax_l1_norm_rows(q_bits, k_bits, softmax_lse, rows: Iterable[int], *, dtype: str,
                          sparse_indices=None, topk_length=None, cu_seqlens_q=None,
                          cu_seqlens_k=None, softmax_scale: float = 1.0, max_seqlen_k: int = 0,
-                         mask_mode: int = 0, layout: str = "BSND") -> np.ndarray:
+                         mask_mode: int = 0, layout: str = "BSND", seqused_q=None,
+                         seqused_k=None) -> np.ndarray:
     """The operator for selected query tokens only; returns float32 (len(rows), width).
 
     ``rows`` are token indices (b*S1 + r for BSND, the packed index for TND).
@@ -220,7 +243,7 @@ def softmax_l1_norm_rows(q_bits, k_bits, softmax_lse, rows: Iterable[int], *, dt
     out = np.zeros((len(rows), width), dtype=np.float32)
     for n, t in enumerate(rows):
         q_row, sel_k, valid = _row_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length,
-                                         width, mask_mode)
+                                         width, mask_mode, seqused_q, seqused_k)
         p = simple_softmax(q_row, sel_k, valid, lse[t], softmax_scale)      # stage 2
         out[n] = reduce_sum_g_mean(p).astype(np.float32)                    # stage 3 (R10)
     return out
@@ -229,7 +252,7 @@ def softmax_l1_norm_rows(q_bits, k_bits, softmax_lse, rows: Iterable[int], *, dt
 def softmax_l1_norm(q_bits, k_bits, softmax_lse, *, dtype: str, sparse_indices=None,
                     topk_length=None, cu_seqlens_q=None, cu_seqlens_k=None,
                     softmax_scale: float = 1.0, max_seqlen_k: int = 0, mask_mode: int = 0,
-                    layout: str = "BSND") -> np.ndarray:
+                    layout: str = "BSND", seqused_q=None, seqused_k=None) -> np.ndarray:
     """The whole operator.  Output float32 (B,S1,1,width) or (T1,1,width)
     ([SMLA] infershape: BSND gives (B, S1, N2, K or S2); TND reading R4)."""
     q_bits = np.asarray(q_bits)
@@ -238,7 +261,8 @@ def softmax_l1_norm(q_bits, k_bits, softmax_lse, *, dtype: str, sparse_indices=N
                                sparse_indices=sparse_indices, topk_length=topk_length,
                                cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
                                softmax_scale=softmax_scale, max_seqlen_k=max_seqlen_k,
-                               mask_mode=mask_mode, layout=layout)
+                               mask_mode=mask_mode, layout=layout, seqused_q=seqused_q,
+                               seqused_k=seqused_k)
     if layout == "TND":
         return out.reshape(n_tok, 1, -1)
     return out.reshape(q_bits.shape[0], q_bits.shape[1], 1, -1)
@@ -250,7 +274,7 @@ def softmax_l1_norm(q_bits, k_bits, softmax_lse, *, dtype: str, sparse_indices=N
 def softmax_lse(q_bits, k_bits, *, dtype: str, rows: Optional[Iterable[int]] = None,
                 sparse_indices=None, topk_length=None, cu_seqlens_q=None, cu_seqlens_k=None,
                 softmax_scale: float = 1.0, max_seqlen_k: int = 0, mask_mode: int = 0,
-                layout: str = "BSND") -> np.ndarray:
+                layout: str = "BSND", seqused_q=None, seqused_k=None) -> np.ndarray:
     """softmaxLse of the forward attention pass over the same valid set:
     lse[t, g] = log sum_{valid i} exp(scale * q[t,g] . k[j_i]), float64,
     -inf for a row with no valid slot.  ([SMLA] 参数说明: softmax_lse is the
@@ -263,7 +287,7 @@ def softmax_lse(q_bits, k_bits, *, dtype: str, rows: Optional[Iterable[int]] = N
     out = np.full((len(rows), G), -math.inf, dtype=np.float64)
     for n, t in enumerate(rows):
         q_row, sel_k, valid = _row_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length,
-                                         width, mask_mode)
+                                         width, mask_mode, seqused_q, seqused_k)
         if not valid.any():
             continue
         x = (q_row @ sel_k[valid].T) * float(softmax_scale)

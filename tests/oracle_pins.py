@@ -367,6 +367,52 @@ def pin_head_symmetries(o):
     _close(outh, base, rtol=2e-7, what="head permutation")
 
 
+def pin_seqused_truncation(o):
+    """seqused_q / seqused_k (reading R11) equal running the operator on the
+    truncated sequences -- the first seqused_q queries and first seqused_k
+    keys of each batch entry, packed as TND -- with the dropped query rows 0;
+    seqused equal to the full lengths changes nothing."""
+    cases = [
+        dict(layout="BSND", dtype="bf16", B=3, S1=9, S2=12, G=3, topk=7, mask_mode=3, seed=500),
+        dict(layout="BSND", dtype="fp16", B=2, S1=8, S2=10, G=2, topk=0, mask_mode=3, seed=501),
+        dict(layout="TND", dtype="bf16", seqlens_q=[6, 9], seqlens_k=[8, 9], G=2, topk=6, mask_mode=3, seed=502),
+        dict(layout="TND", dtype="fp16", seqlens_q=[5, 7], seqlens_k=[9, 7], G=4, topk=0, mask_mode=0, seed=503),
+    ]
+    for ci, case in enumerate(cases):
+        w = W.make_workload(lse=None, **case)
+        rng = np.random.Generator(np.random.PCG64(600 + ci))
+        W.set_lse_rows(w, rng.uniform(0.5, 3.0, size=(w.n_tokens, w.G)).astype(np.float32))
+        seqs = list(w.sequences())
+        su_q = np.array([int(rng.integers(0, Sq + 2)) for (_, _, Sq, _, _) in seqs], dtype=np.int32)
+        su_k = np.array([int(rng.integers(0, Sk + 2)) for (_, _, _, _, Sk) in seqs], dtype=np.int32)
+        full_q = np.array([Sq for (_, _, Sq, _, _) in seqs], dtype=np.int32)
+        full_k = np.array([Sk for (_, _, _, _, Sk) in seqs], dtype=np.int32)
+        base = o.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **kw(w)).reshape(w.n_tokens, -1)
+        same = o.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, seqused_q=full_q, seqused_k=full_k,
+                                 **kw(w)).reshape(w.n_tokens, -1)
+        assert np.array_equal(base, same), "seqused = full lengths must change nothing"
+        got = o.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, seqused_q=su_q, seqused_k=su_k,
+                                **kw(w)).reshape(w.n_tokens, -1)
+        width = w.out_width
+        lse_rows = w.lse_rows()
+        for b, q0, Sq, k0, Sk in seqs:
+            sq, sk = min(Sq, int(su_q[b])), min(Sk, int(su_k[b]))
+            assert np.all(got[q0 + sq:q0 + Sq] == 0.0), f"case {ci} seq {b}: unused rows must be 0"
+            if sq == 0:
+                continue
+            qb = w.q_bits.reshape(w.n_tokens, w.G, D)[q0:q0 + sq]
+            kb = w.k_bits.reshape(-1, 1, D)[k0:k0 + sk] if sk > 0 else np.zeros((0, 1, D), np.uint16)
+            sub = dict(dtype=w.dtype, softmax_scale=w.softmax_scale, mask_mode=w.mask_mode, layout="TND",
+                       cu_seqlens_q=np.array([0, sq], np.int32), cu_seqlens_k=np.array([0, sk], np.int32),
+                       max_seqlen_k=width)
+            if w.sparse_indices is not None:
+                sub["sparse_indices"] = w.sparse_indices.reshape(w.n_tokens, 1, -1)[q0:q0 + sq]
+                if w.topk_length is not None:
+                    sub["topk_length"] = w.topk_length.reshape(w.n_tokens, 1)[q0:q0 + sq]
+            want = o.softmax_l1_norm(qb, kb, lse_rows[q0:q0 + sq].reshape(1, sq, w.G), **sub).reshape(sq, -1)
+            assert np.array_equal(got[q0:q0 + sq], want), f"case {ci} seq {b}: truncated run differs"
+
+
 ALL_PINS = [pin_hand_sparse, pin_hand_causal, pin_row_sums, pin_g1_textbook_softmax,
             pin_brute_force, pin_sparse_equals_dense, pin_layout_equivalence,
-            pin_head_symmetries]
+            pin_head_symmetries, pin_seqused_truncation]

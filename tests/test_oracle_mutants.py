@@ -117,10 +117,30 @@ def _mut_lse_no_scale(m):
     m.softmax_lse = f
 
 
+def _mut_seqused_q_ignored(m):
+    orig = m._effective
+    m._effective = lambda g, sq, sk: orig(g, None, sk)
+
+
+def _mut_seqused_causal_full_lengths(m):
+    """seqused applied to the masks but the causal offset kept on full lengths"""
+    orig_valid = m.slot_valid
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
+        return orig_valid(j, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=topk_len)
+    m.slot_valid = f
+    orig_eff = m._effective
+    def eff(g, sq, sk):
+        b, r, Sq, k0, Sk = orig_eff(g, sq, sk)
+        b0, r0, Sq0, k00, Sk0 = g
+        return b, r, Sq0, k0, Sk       # keeps the full query length for the offset
+    m._effective = eff
+
+
 MUTANTS = [_mut_drop_scale, _mut_sign, _mut_sum_not_mean, _mut_divide_by_slots,
            _mut_causal_off_by_one, _mut_causal_top_left, _mut_ignore_topk_length,
            _mut_mask_on_slot, _mut_lse_head_order, _mut_tnd_key_offset,
-           _mut_keep_out_of_range, _mut_log2, _mut_lse_no_scale]
+           _mut_keep_out_of_range, _mut_log2, _mut_lse_no_scale, _mut_seqused_q_ignored,
+           _mut_seqused_causal_full_lengths]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__[5:])
