@@ -271,6 +271,30 @@ def pin_brute_force(o):
         _close(out.reshape(w.n_tokens, -1), want, rtol=2e-7, atol=1e-30, what="brute force")
 
 
+def pin_lse_logsumexp(o):
+    """softmax_lse equals scipy.special.logsumexp of scale * q.k over the
+    valid set written out by hand (every head separately), and -inf for a row
+    with no valid slot.  One extra case draws topk_length below the number of
+    valid indices, so that it cuts real keys."""
+    cut = W.make_workload(layout="BSND", dtype="bf16", B=2, S1=6, S2=12, G=3, topk=8, mask_mode=0,
+                          seed=109, lse=None)
+    rng = np.random.Generator(np.random.PCG64(109))
+    cut.topk_length = rng.integers(0, 9, size=cut.topk_length.shape).astype(np.int32)
+    for w in tiny_cases() + [cut]:
+        V, J = _valid_by_hand(w)
+        qf = W.half_bits_to_f32(w.q_bits, w.dtype).astype(np.float64).reshape(w.n_tokens, w.G, -1)
+        kf = W.half_bits_to_f32(w.k_bits, w.dtype).astype(np.float64).reshape(-1, qf.shape[2])
+        got = o.softmax_lse(w.q_bits, w.k_bits, **kw(w))
+        assert got.shape == (w.n_tokens, w.G)
+        for t in range(w.n_tokens):
+            v = np.flatnonzero(V[t])
+            if len(v) == 0:
+                assert np.all(np.isneginf(got[t])), f"row {t}: no valid slot, lse {got[t]}"
+                continue
+            x = w.softmax_scale * (qf[t] @ kf[J[t, v]].T)          # (G, n)
+            _close(got[t], scipy.special.logsumexp(x, axis=1), rtol=1e-12, what="lse logsumexp")
+
+
 def pin_sparse_equals_dense(o):
     """Selecting every visible key in ascending order makes the sparse form
     equal the dense form column for column; a random selection, scattered back
@@ -395,6 +419,7 @@ def pin_seqused_truncation(o):
                                 **kw(w)).reshape(w.n_tokens, -1)
         width = w.out_width
         lse_rows = w.lse_rows()
+        lse_cut = o.softmax_lse(w.q_bits, w.k_bits, seqused_q=su_q, seqused_k=su_k, **kw(w))
         for b, q0, Sq, k0, Sk in seqs:
             sq, sk = min(Sq, int(su_q[b])), min(Sk, int(su_k[b]))
             assert np.all(got[q0 + sq:q0 + Sq] == 0.0), f"case {ci} seq {b}: unused rows must be 0"
@@ -411,8 +436,13 @@ def pin_seqused_truncation(o):
                     sub["topk_length"] = w.topk_length.reshape(w.n_tokens, 1)[q0:q0 + sq]
             want = o.softmax_l1_norm(qb, kb, lse_rows[q0:q0 + sq].reshape(1, sq, w.G), **sub).reshape(sq, -1)
             assert np.array_equal(got[q0:q0 + sq], want), f"case {ci} seq {b}: truncated run differs"
+            lse_want = o.softmax_lse(qb, kb, **sub)
+            assert np.array_equal(lse_cut[q0:q0 + sq], lse_want), f"case {ci} seq {b}: truncated lse differs"
+        for b, q0, Sq, k0, Sk in seqs:
+            sq = min(Sq, int(su_q[b]))
+            assert np.all(np.isneginf(lse_cut[q0 + sq:q0 + Sq])), f"case {ci} seq {b}: unused rows' lse"
 
 
 ALL_PINS = [pin_hand_sparse, pin_hand_causal, pin_row_sums, pin_g1_textbook_softmax,
             pin_brute_force, pin_sparse_equals_dense, pin_layout_equivalence,
-            pin_head_symmetries, pin_seqused_truncation]
+            pin_head_symmetries, pin_seqused_truncation, pin_lse_logsumexp]

@@ -136,11 +136,38 @@ def _mut_seqused_causal_full_lengths(m):
     m._effective = eff
 
 
+def _mut_lse_base2(m):
+    """the forward LSE reported in base 2"""
+    orig = m.softmax_lse
+    m.softmax_lse = lambda *a, **k: orig(*a, **k) / np.log(2.0)
+
+
+def _mut_lse_drops_topk_length(m):
+    """the forward LSE taken over every slot, ignoring topk_length"""
+    orig = m.softmax_lse
+    def f(*a, **k):
+        k = dict(k)
+        k["topk_length"] = None
+        return orig(*a, **k)
+    m.softmax_lse = f
+
+
+def _mut_lse_mask_off(m):
+    """the forward LSE taken without the causal mask"""
+    orig = m.softmax_lse
+    def f(*a, **k):
+        k = dict(k)
+        k["mask_mode"] = 0
+        return orig(*a, **k)
+    m.softmax_lse = f
+
+
 MUTANTS = [_mut_drop_scale, _mut_sign, _mut_sum_not_mean, _mut_divide_by_slots,
            _mut_causal_off_by_one, _mut_causal_top_left, _mut_ignore_topk_length,
            _mut_mask_on_slot, _mut_lse_head_order, _mut_tnd_key_offset,
            _mut_keep_out_of_range, _mut_log2, _mut_lse_no_scale, _mut_seqused_q_ignored,
-           _mut_seqused_causal_full_lengths]
+           _mut_seqused_causal_full_lengths, _mut_lse_base2, _mut_lse_drops_topk_length,
+           _mut_lse_mask_off]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__[5:])
