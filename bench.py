@@ -387,6 +387,43 @@ def run_ours(args, world, rank, local):
                "d2h_bytes_per_step": int(sizes.out_bytes), "steps": e_steps,
                "ms_per_step": 1000 * e2e_s / e_steps}
 
+    # ------------------------------------------------ the forward-LSE modes (outside the timed region)
+    lse_modes = None
+    if not args.no_lse_modes:
+        lse_buf = torch.empty(plan.lse_shape, dtype=torch.float32, device=device)
+        extra = dict(sparse_indices=dev["indices"], topk_length=dev["topk_length"], stream=stream)
+        modes = {
+            "lse_forward": (lambda: plan.softmax_lse(dev["q"], dev["k"], lse_out=lse_buf, **extra), 1),
+            "lse_then_l1norm_fused": (lambda: plan.run_fused_lse(dev["q"], dev["k"], out=out, lse_out=lse_buf,
+                                                                 **extra), 2),
+        }
+        lse_modes = {}
+        _, bf16_peak, peak_src = load_peaks()
+        for mname, (fn, passes) in modes.items():
+            for _ in range(3):
+                flush.zero_()
+                fn()
+            torch.cuda.synchronize(device)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.lse_steps)]
+            for a, b in ev:
+                flush.zero_()
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize(device)
+            code, flags = plan.status(stream)
+            if code != smla.SMLA_OK:
+                raise RuntimeError(f"device status {code} flags {flags} in mode {mname}")
+            ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+            ms = all_max(ms, world, device)
+            tf = passes * flops / (ms / 1000.0) / 1e12
+            lse_modes[mname] = {"ms_per_launch": ms, "launches": args.lse_steps,
+                                "pairs_per_s": world * pairs / (ms / 1000.0), "tflops": tf,
+                                "mma_passes": passes,
+                                "roofline_tensor": {"achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                                                    "frac": tf / bf16_peak, "peak_source": peak_src}}
+
     if rank != 0:
         return 0
 
@@ -430,6 +467,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": args.steps,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "lse_modes": lse_modes,
         "wall_s_timed_region": wall,
         "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "stages", "mma_n",
                                                                         "smem_bytes", "max_cta_cost",
@@ -451,6 +489,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--no-lse-modes", action="store_true",
+                    help="skip timing the forward-LSE and fused LSE+L1-norm launches")
+    ap.add_argument("--lse-steps", type=int, default=50)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -187,6 +187,74 @@ smla_status smla_l1norm_run(const smla_plan *plan, const void *q, const void *k,
                             const float *softmax_lse, const int32_t *sparse_indices,
                             const int32_t *topk_length, float *out, smla_stream_t stream);
 
+/*
+ * The tensors of one call, for smla_l1norm_run_tensors().  Device pointers;
+ * the first five and ``out`` as for smla_l1norm_run().  The two optional
+ * inputs of the article's parameter table (参数说明) that run() has no slot
+ * for:
+ *
+ *   seqused_q   (B,) int32 or NULL: query tokens of each sequence that take
+ *               part.  Sequence b's query rows r >= min(Sq_b, seqused_q[b])
+ *               are written as all-zero rows.  Negative values count as 0.
+ *   seqused_k   (B,) int32 or NULL: keys of each sequence that take part.
+ *               Key positions j >= min(Sk_b, seqused_k[b]) are masked (0).
+ *
+ * With either given, mask_mode 3 places the causal diagonal on the cut
+ * lengths: row r sees key j iff j <= r + Sk' - Sq', Sq' and Sk' being the
+ * lengths after the cut.  B is batch_size (the number of sequences in TND).
+ * The values are read on the device, so the plan's work schedule is balanced
+ * on the full lengths; the cut only removes work.  An index in [Sk', Sk) is
+ * masked without raising the bad-index warning.
+ */
+typedef struct {
+  const void *q;
+  const void *k;
+  const float *softmax_lse;
+  const int32_t *sparse_indices;
+  const int32_t *topk_length;
+  const int32_t *seqused_q;
+  const int32_t *seqused_k;
+  float *out;
+} smla_l1norm_tensors;
+
+/* smla_l1norm_run() with every optional input; same errors (NULL ``tensors``
+ * is SMLA_ERR_NULLPTR; a seqused pointer that is not 4-byte aligned is
+ * SMLA_ERR_INVALID).  run() is this call with both seqused pointers NULL. */
+smla_status smla_l1norm_run_tensors(const smla_plan *plan, const smla_l1norm_tensors *tensors,
+                                    smla_stream_t stream);
+
+/*
+ * The forward pass's softmax_lse, computed on the GPU over the same kept
+ * slots the operator uses (article "SparseFlashMlaSoftmaxL1Norm", 参数说明:
+ * softmax_lse is the output of the forward attention pass; in the section
+ * 三阶段计算公式, stage 2's SimpleSoftmax normalises by it):
+ *
+ *   lse_out[row, g] = log sum_{kept slots i} exp(scale * q[row, g] . K[j_i])
+ *
+ * natural logarithm, fp32, -inf for a row with no kept slot.  ``lse_out``
+ * has the layout of softmax_lse: (B,1,S1,G) or (1,T1,G), i.e. token-major
+ * (token, g); device pointer, 4-byte aligned.  One launch of the same
+ * persistent kernel in a mode where the MMA puts the q rows on M and the
+ * keys on N and each epilogue thread keeps a running maximum and sum for its
+ * row.  Reads q, k, sparse_indices, topk_length and the seqused tensors of
+ * ``tensors``; ignores softmax_lse and out.  Same errors as
+ * smla_l1norm_run_tensors() (``lse_out`` NULL: SMLA_ERR_NULLPTR).
+ */
+smla_status smla_softmax_lse_run(const smla_plan *plan, const smla_l1norm_tensors *tensors,
+                                 float *lse_out, smla_stream_t stream);
+
+/*
+ * Both in one launch: for each work item, a pass over its key tiles
+ * computes the LSE as smla_softmax_lse_run() does and writes it to
+ * ``lse_out``, then a second pass over the same tiles (the keys gathered
+ * again) computes the operator with that LSE and writes ``tensors->out``.
+ * The q block stays in shared memory for both passes.  Ignores
+ * tensors->softmax_lse.  Each output row over its kept slots sums to 1 up
+ * to rounding.
+ */
+smla_status smla_l1norm_run_fused_lse(const smla_plan *plan, const smla_l1norm_tensors *tensors,
+                                      float *lse_out, smla_stream_t stream);
+
 /* Host-side sizes, in bytes, of the tensors run() reads and writes. */
 typedef struct {
   size_t q_bytes, k_bytes, lse_bytes, indices_bytes, topk_length_bytes, out_bytes;
@@ -224,7 +292,7 @@ smla_status smla_l1norm_get_status(const smla_plan *plan, smla_stream_t stream, 
  * call.  If ``items`` is non-NULL it receives up to ``items_capacity`` work
  * items of 8 int32 each, grouped by CTA (fields: first token, tokens in the
  * item, local row of the first token, first key row of the sequence, Sq, Sk,
- * key tiles of a dense item, reserved); ``cta_offsets`` (num_ctas + 1 int32)
+ * key tiles of a dense item, sequence number b); ``cta_offsets`` (num_ctas + 1 int32)
  * receives where each CTA's items start.  ``info`` receives the summary.
  */
 smla_status smla_l1norm_schedule_host(const smla_l1norm_desc *desc, int32_t num_ctas,

@@ -69,6 +69,11 @@ class PlanInfo(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
 
+class _Tensors(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("q", "k", "softmax_lse", "sparse_indices", "topk_length", "seqused_q", "seqused_k", "out")]
+
+
 class IoSizes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("q_bytes", "k_bytes", "lse_bytes", "indices_bytes", "topk_length_bytes", "out_bytes")]
@@ -104,6 +109,12 @@ def library():
     lib.smla_l1norm_plan_get_info.restype = I32
     lib.smla_l1norm_run.argtypes = [P, P, P, P, P, P, P, P]
     lib.smla_l1norm_run.restype = I32
+    lib.smla_l1norm_run_tensors.argtypes = [P, ctypes.POINTER(_Tensors), P]
+    lib.smla_l1norm_run_tensors.restype = I32
+    lib.smla_softmax_lse_run.argtypes = [P, ctypes.POINTER(_Tensors), P, P]
+    lib.smla_softmax_lse_run.restype = I32
+    lib.smla_l1norm_run_fused_lse.argtypes = [P, ctypes.POINTER(_Tensors), P, P]
+    lib.smla_l1norm_run_fused_lse.restype = I32
     lib.smla_l1norm_io_sizes.argtypes = [P, ctypes.POINTER(IoSizes)]
     lib.smla_l1norm_io_sizes.restype = I32
     lib.smla_l1norm_run_from_host.argtypes = [P] + [P] * 6 + [P] * 6 + [P]
@@ -253,17 +264,74 @@ class Plan:
         _check(self._lib.smla_l1norm_io_sizes(self._h, ctypes.byref(s)), "io_sizes")
         return s
 
-    def run(self, q, k, softmax_lse, sparse_indices=None, topk_length=None, out=None, stream=None):
-        """``smla_l1norm_run``; allocates ``out`` (fp32) if not given."""
+    def run(self, q, k, softmax_lse, sparse_indices=None, topk_length=None, out=None, stream=None,
+            seqused_q=None, seqused_k=None):
+        """``smla_l1norm_run`` (``smla_l1norm_run_tensors`` when ``seqused_q`` or
+        ``seqused_k`` is given: int32 CUDA tensors of one value per sequence);
+        allocates ``out`` (fp32) if not given."""
         if out is None:
             import torch
             out = torch.empty(self.output_shape, dtype=torch.float32, device=q.device)
-        code = self._lib.smla_l1norm_run(
-            self._h, _ptr(q, "q"), _ptr(k, "k", required=False), _ptr(softmax_lse, "softmax_lse"),
-            _ptr(sparse_indices, "sparse_indices", required=False),
-            _ptr(topk_length, "topk_length", required=False), _ptr(out, "out"), _stream_handle(stream))
-        _check(code, "smla_l1norm_run")
+        if seqused_q is None and seqused_k is None:
+            code = self._lib.smla_l1norm_run(
+                self._h, _ptr(q, "q"), _ptr(k, "k", required=False), _ptr(softmax_lse, "softmax_lse"),
+                _ptr(sparse_indices, "sparse_indices", required=False),
+                _ptr(topk_length, "topk_length", required=False), _ptr(out, "out"), _stream_handle(stream))
+            _check(code, "smla_l1norm_run")
+            return out
+        t = _Tensors(_ptr(q, "q"), _ptr(k, "k", required=False), _ptr(softmax_lse, "softmax_lse"),
+                     _ptr(sparse_indices, "sparse_indices", required=False),
+                     _ptr(topk_length, "topk_length", required=False),
+                     _ptr(seqused_q, "seqused_q", required=False),
+                     _ptr(seqused_k, "seqused_k", required=False), _ptr(out, "out"))
+        code = self._lib.smla_l1norm_run_tensors(self._h, ctypes.byref(t), _stream_handle(stream))
+        _check(code, "smla_l1norm_run_tensors")
         return out
+
+    @property
+    def lse_shape(self) -> tuple:
+        """Shape of softmax_lse: (B, 1, S1, G) or (1, T1, G)."""
+        d = self.desc_kwargs
+        G = int(d["num_heads_q"]) // int(d.get("num_heads_k", 1))
+        if d.get("layout", "BSND") == "TND":
+            return (1, int(self.info.num_tokens), G)
+        return (int(d.get("batch_size", 0)), 1, int(d.get("max_seqlen_q", 0)), G)
+
+    def _tensors(self, q, k, sparse_indices, topk_length, seqused_q, seqused_k, out):
+        return _Tensors(_ptr(q, "q"), _ptr(k, "k", required=False), None,
+                        _ptr(sparse_indices, "sparse_indices", required=False),
+                        _ptr(topk_length, "topk_length", required=False),
+                        _ptr(seqused_q, "seqused_q", required=False),
+                        _ptr(seqused_k, "seqused_k", required=False), _ptr(out, "out", required=False))
+
+    def softmax_lse(self, q, k, sparse_indices=None, topk_length=None, lse_out=None, stream=None,
+                    seqused_q=None, seqused_k=None):
+        """``smla_softmax_lse_run``: the forward LSE over the kept slots
+        (natural log, fp32, -inf for a row with none); allocates ``lse_out``
+        if not given."""
+        if lse_out is None:
+            import torch
+            lse_out = torch.empty(self.lse_shape, dtype=torch.float32, device=q.device)
+        t = self._tensors(q, k, sparse_indices, topk_length, seqused_q, seqused_k, None)
+        code = self._lib.smla_softmax_lse_run(self._h, ctypes.byref(t), _ptr(lse_out, "lse_out"),
+                                              _stream_handle(stream))
+        _check(code, "smla_softmax_lse_run")
+        return lse_out
+
+    def run_fused_lse(self, q, k, sparse_indices=None, topk_length=None, out=None, lse_out=None,
+                      stream=None, seqused_q=None, seqused_k=None):
+        """``smla_l1norm_run_fused_lse``: the forward LSE and the operator
+        from it in one launch; returns (out, lse_out)."""
+        import torch
+        if out is None:
+            out = torch.empty(self.output_shape, dtype=torch.float32, device=q.device)
+        if lse_out is None:
+            lse_out = torch.empty(self.lse_shape, dtype=torch.float32, device=q.device)
+        t = self._tensors(q, k, sparse_indices, topk_length, seqused_q, seqused_k, out)
+        code = self._lib.smla_l1norm_run_fused_lse(self._h, ctypes.byref(t), _ptr(lse_out, "lse_out"),
+                                                   _stream_handle(stream))
+        _check(code, "smla_l1norm_run_fused_lse")
+        return out, lse_out
 
     def run_from_host(self, h, d, stream=None):
         """``smla_l1norm_run_from_host``: ``h`` and ``d`` map the roles
@@ -315,14 +383,16 @@ _PLAN_CACHE = {}
 
 
 def sparse_flash_mla_softmax_l1_norm(q, k, softmax_lse, *, sparse_indices=None, cu_seqlens_q=None,
-                                     cu_seqlens_k=None, topk_length=None, softmax_scale: float = 1.0,
+                                     cu_seqlens_k=None, seqused_q=None, seqused_k=None,
+                                     topk_length=None, softmax_scale: float = 1.0,
                                      max_seqlen_k: int = 0, cmp_ratio: int = 1, mask_mode: int = 0,
                                      layout_q: str = "BSND", layout_k: str = "BSND",
                                      stream=None):
     """Functional form with the article's PyTorch argument names.  ``q``, ``k``,
     ``softmax_lse`` and the optional int32 tensors are CUDA tensors;
     ``cu_seqlens_q/k`` may be CUDA or CPU tensors or sequences (they are read
-    on the host to build the schedule).  Plans are cached per shape."""
+    on the host to build the schedule); ``seqused_q/k`` are int32 CUDA
+    tensors, read on the device.  Plans are cached per shape."""
     import torch
     if layout_q != layout_k:
         raise ValueError("layout_q must equal layout_k")
@@ -350,4 +420,5 @@ def sparse_flash_mla_softmax_l1_norm(q, k, softmax_lse, *, sparse_indices=None, 
                     softmax_scale=softmax_scale, has_topk_length=topk_length is not None,
                     cu_seqlens_q=cq, cu_seqlens_k=ck)
         _PLAN_CACHE[key] = plan
-    return plan.run(q, k, softmax_lse, sparse_indices=sparse_indices, topk_length=topk_length, stream=stream)
+    return plan.run(q, k, softmax_lse, sparse_indices=sparse_indices, topk_length=topk_length, stream=stream,
+                    seqused_q=seqused_q, seqused_k=seqused_k)

@@ -165,7 +165,7 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
         if (Sk == 0) n = 0;
         const int64_t tiles = ceil_div(n, smla::kTileKeys);
         WorkItem w{static_cast<int32_t>(tok), 1, static_cast<int32_t>(r), static_cast<int32_t>(g.k0[b]),
-                   static_cast<int32_t>(Sq), static_cast<int32_t>(Sk), 0, 0};
+                   static_cast<int32_t>(Sq), static_cast<int32_t>(Sk), 0, b};
         items.push_back(w);
         cost.push_back(static_cast<double>(tiles) + row_overhead +
                        0.02 * static_cast<double>(g.width - tiles * smla::kTileKeys) / smla::kTileKeys);
@@ -178,7 +178,7 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
         const int64_t tiles = ceil_div(std::min<int64_t>(vis, g.width), smla::kTileKeys);
         WorkItem w{static_cast<int32_t>(g.q0[b] + r0), static_cast<int32_t>(nrows), static_cast<int32_t>(r0),
                    static_cast<int32_t>(g.k0[b]), static_cast<int32_t>(Sq), static_cast<int32_t>(Sk),
-                   static_cast<int32_t>(tiles), 0};
+                   static_cast<int32_t>(tiles), b};
         items.push_back(w);
         cost.push_back(static_cast<double>(tiles) + row_overhead +
                        0.02 * nrows * static_cast<double>(g.width - tiles * smla::kTileKeys) / smla::kTileKeys);
@@ -459,35 +459,52 @@ smla_status smla_l1norm_io_sizes(const smla_plan* plan, smla_io_sizes* s) {
   return SMLA_OK;
 }
 
-smla_status smla_l1norm_run(const smla_plan* plan, const void* q, const void* k, const float* softmax_lse,
-                            const int32_t* sparse_indices, const int32_t* topk_length, float* out,
-                            smla_stream_t stream) {
-  if (plan == nullptr) return SMLA_ERR_NULLPTR;
+}  // extern "C"
+
+namespace {
+
+// Checks the tensors a mode needs and launches it.  kModeL1 reads
+// t->softmax_lse and writes t->out; kModeLse writes lse_out only; kModeFused
+// writes lse_out and t->out.
+smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, float* lse_out, int mode,
+                        smla_stream_t stream) {
+  if (plan == nullptr || t == nullptr) return SMLA_ERR_NULLPTR;
   const Geometry& g = plan->geo;
-  if (g.n_tokens == 0 || g.width == 0) return SMLA_OK;  // empty q (or empty output): nothing to do
-  if (q == nullptr || softmax_lse == nullptr || out == nullptr) return SMLA_ERR_NULLPTR;
-  if (g.k_rows > 0 && k == nullptr) return SMLA_ERR_NULLPTR;
-  if (g.sparse && sparse_indices == nullptr) return SMLA_ERR_NULLPTR;
-  if (plan->desc.has_topk_length && topk_length == nullptr) return SMLA_ERR_NULLPTR;
-  if (!aligned16(q) || (k != nullptr && !aligned16(k)) || !aligned4(softmax_lse) || !aligned4(out) ||
-      (sparse_indices != nullptr && !aligned4(sparse_indices)) || (topk_length != nullptr && !aligned4(topk_length)))
-    return SMLA_ERR_INVALID;
+  if (g.n_tokens == 0) return SMLA_OK;                       // empty q: nothing to do
+  if (mode == smla::kModeL1 && g.width == 0) return SMLA_OK;  // empty output
+  const bool wants_out = mode != smla::kModeLse;
+  const bool wants_lse_in = mode == smla::kModeL1;
+  if (t->q == nullptr) return SMLA_ERR_NULLPTR;
+  if (wants_out && t->out == nullptr) return SMLA_ERR_NULLPTR;
+  if (wants_lse_in && t->softmax_lse == nullptr) return SMLA_ERR_NULLPTR;
+  if (!wants_lse_in && lse_out == nullptr) return SMLA_ERR_NULLPTR;
+  if (g.k_rows > 0 && t->k == nullptr) return SMLA_ERR_NULLPTR;
+  if (g.sparse && t->sparse_indices == nullptr) return SMLA_ERR_NULLPTR;
+  if (plan->desc.has_topk_length && t->topk_length == nullptr) return SMLA_ERR_NULLPTR;
+  if (!aligned16(t->q) || (t->k != nullptr && !aligned16(t->k))) return SMLA_ERR_INVALID;
+  const void* a4[] = {wants_lse_in ? t->softmax_lse : nullptr, wants_out ? t->out : nullptr, lse_out,
+                      t->sparse_indices, t->topk_length, t->seqused_q, t->seqused_k};
+  for (const void* a : a4)
+    if (a != nullptr && !aligned4(a)) return SMLA_ERR_INVALID;
 
   CUtensorMap tq;
   const int q_box = g.R * g.G;
-  if (!encode_rows_map(&tq, q, g.q_rows, q_box, plan->desc.dtype)) {
+  if (!encode_rows_map(&tq, t->q, g.q_rows, q_box, plan->desc.dtype)) {
     g_last_cuda_error = "cuTensorMapEncodeTiled(q) failed";
     return SMLA_ERR_CUDA;
   }
   smla::KernelParams p{};
-  p.k = static_cast<const uint8_t*>(k);  // unread when there is no key row (every item has zero tiles)
+  p.k = static_cast<const uint8_t*>(t->k);  // unread when there is no key row (every item has zero tiles)
   p.items = plan->d_items;
   p.cta_begin = plan->d_cta_begin;
   p.status = plan->d_status;
-  p.lse = softmax_lse;
-  p.idx = g.sparse ? sparse_indices : nullptr;
-  p.topk_len = plan->desc.has_topk_length ? topk_length : nullptr;
-  p.out = out;
+  p.lse = wants_lse_in ? t->softmax_lse : nullptr;
+  p.idx = g.sparse ? t->sparse_indices : nullptr;
+  p.topk_len = plan->desc.has_topk_length ? t->topk_length : nullptr;
+  p.seqused_q = t->seqused_q;
+  p.seqused_k = t->seqused_k;
+  p.out = wants_out ? t->out : nullptr;
+  p.lse_out = wants_lse_in ? nullptr : lse_out;
   p.G = g.G;
   p.R = g.R;
   p.n_mma = g.n_mma;
@@ -497,13 +514,39 @@ smla_status smla_l1norm_run(const smla_plan* plan, const void* q, const void* k,
   p.mask_mode = plan->desc.mask_mode;
   p.stages = plan->stages;
   p.idesc = static_cast<int32_t>(plan->idesc);
+  p.idesc_lse = static_cast<int32_t>(make_idesc(plan->desc.dtype, smla::kTileKeys));
   p.c_log2 = static_cast<float>(static_cast<double>(plan->desc.softmax_scale) * 1.4426950408889634);
   p.inv_g = 1.0f / static_cast<float>(g.G);
   p.timeout_ns = plan->timeout_ns;
-  cudaError_t e = smla::launch_fused(p, tq, g.sparse, plan->num_ctas, plan->smem,
+  cudaError_t e = smla::launch_fused(p, tq, g.sparse, mode, plan->num_ctas, plan->smem,
                                      reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return SMLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+smla_status smla_l1norm_run_tensors(const smla_plan* plan, const smla_l1norm_tensors* t, smla_stream_t stream) {
+  return launch_mode(plan, t, nullptr, smla::kModeL1, stream);
+}
+
+smla_status smla_softmax_lse_run(const smla_plan* plan, const smla_l1norm_tensors* t, float* lse_out,
+                                 smla_stream_t stream) {
+  return launch_mode(plan, t, lse_out, smla::kModeLse, stream);
+}
+
+smla_status smla_l1norm_run_fused_lse(const smla_plan* plan, const smla_l1norm_tensors* t, float* lse_out,
+                                      smla_stream_t stream) {
+  return launch_mode(plan, t, lse_out, smla::kModeFused, stream);
+}
+
+smla_status smla_l1norm_run(const smla_plan* plan, const void* q, const void* k, const float* softmax_lse,
+                            const int32_t* sparse_indices, const int32_t* topk_length, float* out,
+                            smla_stream_t stream) {
+  const smla_l1norm_tensors t{q, k, softmax_lse, sparse_indices, topk_length, nullptr, nullptr, out};
+  return smla_l1norm_run_tensors(plan, &t, stream);
 }
 
 smla_status smla_l1norm_run_from_host(const smla_plan* plan, const void* h_q, const void* h_k, const float* h_lse,

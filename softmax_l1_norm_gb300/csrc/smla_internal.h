@@ -41,8 +41,8 @@ struct WorkItem {
   int32_t k_base;   // global key row of key position 0 of the sequence
   int32_t Sq;       // query length of the sequence
   int32_t Sk;       // key length of the sequence
-  int32_t ntiles;   // dense form: 128-key tiles to compute (the rest is zero)
-  int32_t pad;
+  int32_t ntiles;   // dense form: 128-key tiles to compute on full lengths (the rest is zero)
+  int32_t b;        // batch entry (sequence) of the item
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem is 32 bytes");
 
@@ -54,7 +54,10 @@ struct KernelParams {
   const float* lse;           // (tokens, G)
   const int32_t* idx;         // (tokens, topk) or null
   const int32_t* topk_len;    // (tokens) or null
-  float* out;                 // (tokens, width)
+  const int32_t* seqused_q;   // (batch) participating query rows per sequence, or null
+  const int32_t* seqused_k;   // (batch) participating keys per sequence, or null
+  float* out;                 // (tokens, width); unused by the LSE-only mode
+  float* lse_out;             // (tokens, G) forward LSE written by the LSE modes, else null
   int32_t G;                  // heads per key head
   int32_t R;                  // tokens per item (dense), 1 (sparse)
   int32_t n_mma;              // MMA N = pad16(R*G)
@@ -63,7 +66,8 @@ struct KernelParams {
   int32_t width;              // output row length
   int32_t mask_mode;          // 0 or 3
   int32_t stages;             // key ring depth
-  int32_t idesc;              // tcgen05 instruction descriptor
+  int32_t idesc;              // tcgen05 instruction descriptor: A = keys, B = q (M 128, N n_mma)
+  int32_t idesc_lse;          // the same for the LSE pass: A = q rows, B = keys (M 128, N 128)
   float c_log2;               // softmax_scale * log2(e)
   float inv_g;                // 1 / G
   int64_t timeout_ns;         // bound on every device-side wait
@@ -74,12 +78,19 @@ inline int smem_bytes_for(int n_mma, int stages) {
   const int q_bytes = kNumChunks * n_mma * 128;
   const int ring = stages * kKStageBytes;
   const int bars = (2 * kNumChunks + 2 * kMaxStages + 2 * kAccBufs + 2) * 8;
-  const int tables = kMaxN * 4;  // lse table of the epilogue warpgroup
+  const int tables = kMaxN * 4 + 64;  // lse table and slot masks of the epilogue warpgroup
   return 1024 /* alignment slack */ + q_bytes + ring + bars + tables + 128;
 }
 
+// What one launch computes.
+enum Mode : int {
+  kModeL1 = 0,     // the L1 norm from a given LSE
+  kModeLse = 1,    // the forward LSE only
+  kModeFused = 2,  // the forward LSE, then the L1 norm from it, per work item
+};
+
 // Launch the fused kernel (defined in smla_kernel.cu).
-cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int grid,
+cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int mode, int grid,
                          int smem_bytes, cudaStream_t stream);
 cudaError_t configure_fused(int smem_bytes);
 

@@ -186,17 +186,9 @@ __device__ __forceinline__ uint64_t sdesc_k_major_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
   return d;
 }
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// The same MMA with the descriptors given as (low, high) 32-bit halves and a
-// constant accumulate flag: the issuing thread's per-MMA work is two moves.
+// tcgen05.mma kind::f16 with the descriptors given as (low, high) 32-bit
+// halves and a constant accumulate flag: the issuing thread's per-MMA work is
+// two moves.
 template <bool kAccumulate>
 __device__ __forceinline__ void umma_f16_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                               uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
@@ -259,6 +251,7 @@ __device__ __forceinline__ bool wg_all(int id, bool v) {
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // Roles.
 // Warps are spread over the four SM sub-partitions (warp % 4) so that the
@@ -270,7 +263,6 @@ constexpr int kQWarp = 8;           // sleeps in barrier waits most of the time
 constexpr int kProducerWarps = 4;   // warps 1, 3, 9, 11 (sub-partitions 1 and 3)
 constexpr int kKeysPerLane = kTileKeys / (kProducerWarps * 4);   // 8
 constexpr int kEpiWarp0 = 4;        // warps 4-7: one warpgroup
-constexpr int kEpiGroups = 1;
 __device__ __forceinline__ int producer_index(int warp) {
   switch (warp) {
     case 1: return 0;
@@ -281,34 +273,65 @@ __device__ __forceinline__ int producer_index(int warp) {
   }
 }
 
+// Lengths of an item's sequence that take part in the computation: the
+// full lengths, cut to seqused_q[b] / seqused_k[b] when those are given
+// (query rows at or past Sq are all zero, keys at or past Sk are masked, and
+// the right-down causal diagonal is placed on the cut lengths).
+struct EffLen {
+  int Sq, Sk;
+};
+__device__ __forceinline__ EffLen effective_lengths(const KernelParams& p, const WorkItem& w) {
+  EffLen e{w.Sq, w.Sk};
+  if (p.seqused_q != nullptr) e.Sq = max(0, min(e.Sq, __ldg(p.seqused_q + w.b)));
+  if (p.seqused_k != nullptr) e.Sk = max(0, min(e.Sk, __ldg(p.seqused_k + w.b)));
+  return e;
+}
+
 // Key tiles an item needs, and (sparse form) the clamped topk_length.
 template <bool kSparse>
 __device__ __forceinline__ int item_tiles(const KernelParams& p, const WorkItem& w, int& tl) {
   if (kSparse) {
+    const EffLen e = effective_lengths(p, w);
     int n = p.topk;
     if (p.topk_len != nullptr) n = min(max(__ldg(p.topk_len + w.q_tok), 0), p.topk);
-    if (w.Sk <= 0) n = 0;
+    if (e.Sk <= 0 || w.r0 >= e.Sq) n = 0;
     tl = n;
     return (n + kTileKeys - 1) / kTileKeys;
   }
   tl = 0;
-  return w.ntiles;
+  if (p.seqused_q == nullptr && p.seqused_k == nullptr) return w.ntiles;
+  // keys visible to the item's last participating row, within the output width
+  const EffLen e = effective_lengths(p, w);
+  const int rows = min(w.nrows, e.Sq - w.r0);
+  if (rows <= 0) return 0;
+  int vis = e.Sk;
+  if (p.mask_mode != 0) vis = min(e.Sk, max(0, w.r0 + rows + e.Sk - e.Sq));
+  vis = min(vis, p.width);
+  return (vis + kTileKeys - 1) / kTileKeys;
+}
+
+// Passes over an item's key tiles: the LSE pass, the L1-norm pass, or both.
+template <int kMode>
+__host__ __device__ constexpr int passes() {
+  return kMode == kModeFused ? 2 : 1;
 }
 
 // Position in a CTA's sequence of (item, key tile) pairs, skipping items
-// without tiles.
+// without tiles.  t runs over every pass's tiles; ktile is the key tile.
 struct TileCursor {
-  int it, t, nt, tl;
+  int it, t, nt, ntk, tl;
   WorkItem w;
+  __device__ __forceinline__ int ktile() const { return t < ntk ? t : t - ntk; }
 };
 
-template <bool kSparse>
+template <bool kSparse, int kMode>
 __device__ __forceinline__ bool cursor_next(const KernelParams& p, TileCursor& c, int it1) {
   ++c.t;
   while (c.t >= c.nt) {
     if (++c.it >= it1) return false;
     c.w = p.items[c.it];
-    c.nt = item_tiles<kSparse>(p, c.w, c.tl);
+    c.ntk = item_tiles<kSparse>(p, c.w, c.tl);
+    c.nt = c.ntk * passes<kMode>();
     c.t = 0;
   }
   return true;
@@ -329,14 +352,22 @@ struct MmaCtx {
 // latency behind, so the loop is kept minimal: the descriptors differ only
 // in their low word (start address), the chunk loop is unrolled and the
 // accumulate flag is a constant.
-template <bool kSparse, int H>
+//
+// The L1-norm pass puts the 128 keys of a tile on M (TMEM lanes) and the
+// heads on N, so that an epilogue thread owns one key slot and sums over the
+// heads.  The LSE pass swaps the operands: M = 128 q rows (heads; rows past
+// R*G read neighbouring shared memory and are never used), N = the 128 keys,
+// so that a thread owns one head and reduces over the keys.  Both operands
+// are 128-byte-swizzled K-major tiles, so the swap only exchanges the start
+// addresses and the instruction descriptor.
+template <bool kSparse, int kMode, int H>
 __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m, const WaitCtl& ctl) {
   const uint64_t a0 = sdesc_k_major_sw128(m.sK);
   const uint64_t b0 = sdesc_k_major_sw128(m.sQ);
+  // both descriptors share their high word (strides, version, swizzle)
   const uint32_t a_hi = static_cast<uint32_t>(a0 >> 32), b_hi = static_cast<uint32_t>(b0 >> 32);
-  const uint32_t a_lo0 = static_cast<uint32_t>(a0), b_lo0 = static_cast<uint32_t>(b0);
+  const uint32_t k_lo0 = static_cast<uint32_t>(a0), q_lo0 = static_cast<uint32_t>(b0);
   const uint32_t b_step = static_cast<uint32_t>(m.q_chunk_bytes) >> 4;
-  const uint32_t idesc = static_cast<uint32_t>(p.idesc);
   const uint32_t S = static_cast<uint32_t>(p.stages);
   uint32_t kst = 0, kph = 0, qit = 0, acc = 0;
   bool ok = true;
@@ -348,13 +379,15 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
     const int nt = item_tiles<kSparse>(p, w, tl);
     if (nt == 0) continue;
     const uint32_t qpar = qit & 1u;
-    for (int t = 0; t < nt && ok; ++t, ++acc) {
+    for (int t = 0; t < nt * passes<kMode>() && ok; ++t, ++acc) {
       const uint32_t buf = acc & (kAccBufs - 1);
       ok = wait_bounded(m.bar_acc_empty + 8 * buf, ((acc / kAccBufs) & 1u) ^ 1u, ctl);
       if (!ok) break;
       tc_fence_after();
       const uint32_t d_tmem = m.tmem_base + buf * kAccCols + H * kHalfCols;
-      const bool last = (t == nt - 1);
+      const bool last = (t == nt * passes<kMode>() - 1);
+      const bool lse_pass = kMode != kModeL1 && t < nt;
+      const uint32_t idesc = static_cast<uint32_t>(lse_pass ? p.idesc_lse : p.idesc);
       // ring slot and phase of each of the tile's 8 stages
       uint32_t sl[kNumChunks], ph[kNumChunks];
 #pragma unroll
@@ -384,8 +417,10 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
         // the barrier, become visible to the tensor cores (async proxy)
         fence_proxy_async();
         tc_fence_after();
-        const uint32_t a_lo = a_lo0 + sl[c] * (kKStageBytes >> 4);
-        const uint32_t b_lo = b_lo0 + c * b_step;
+        const uint32_t k_lo = k_lo0 + sl[c] * (kKStageBytes >> 4);
+        const uint32_t q_lo = q_lo0 + c * b_step;
+        const uint32_t a_lo = lse_pass ? q_lo : k_lo;
+        const uint32_t b_lo = lse_pass ? k_lo : q_lo;
         // 4 K-steps of 16 elements (32 bytes) inside the swizzled rows
         if (c == H)
           umma_f16_lohi<false>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc);
@@ -407,7 +442,7 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
 
 }  // namespace
 
-template <bool kSparse>
+template <bool kSparse, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     smla_fused_kernel(const __grid_constant__ KernelParams p,
                       const __grid_constant__ CUtensorMap tmap_q) {
@@ -431,6 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (sMisc - base));
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + (sMisc - base) + 4);
   float* ltab = reinterpret_cast<float*>(gbase + (sMisc - base) + 64);
+  // slot masks of the LSE pass: 4 words (128 slots) per tile, two tiles
+  volatile uint32_t* vmask = reinterpret_cast<volatile uint32_t*>(gbase + (sMisc - base) + 64 + kMaxN * 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -495,13 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t S = static_cast<uint32_t>(p.stages);
     uint32_t kst = 0, kph = 0;   // slot being filled, its phase
     bool ok = true;
-    TileCursor cur{it0 - 1, 0, 0, 0, WorkItem{}};
-    bool have = cursor_next<kSparse>(p, cur, it1);
+    TileCursor cur{it0 - 1, 0, 0, 0, 0, WorkItem{}};
+    bool have = cursor_next<kSparse, kMode>(p, cur, it1);
     int jn[kKeysPerLane];
     auto fetch_indices = [&](const TileCursor& c) {
 #pragma unroll
       for (int i = 0; i < kKeysPerLane; ++i) {
-        const int slot = c.t * kTileKeys + krow0 + 4 * i;
+        const int slot = c.ktile() * kTileKeys + krow0 + 4 * i;
         if (kSparse) {
           jn[i] = slot < c.tl ? __ldg(p.idx + static_cast<int64_t>(c.w.q_tok) * p.topk + slot) : -1;
         } else {
@@ -518,12 +555,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < kKeysPerLane; ++i) {
         const int j = jn[i];
         const bool in = (j >= 0) && (j < cur.w.Sk);
-        if (kSparse) bad |= (krow0 + 4 * i + cur.t * kTileKeys < cur.tl) && !in && (j != -1);
+        if (kSparse) bad |= (krow0 + 4 * i + cur.ktile() * kTileKeys < cur.tl) && !in && (j != -1);
         src[i] = p.k + (static_cast<int64_t>(cur.w.k_base) + (in ? j : 0)) * (kHeadDim * 2) + seg * 16;
       }
       if (kSparse && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kFlagBadIndex);
       TileCursor nxt = cur;
-      const bool have_next = cursor_next<kSparse>(p, nxt, it1);
+      const bool have_next = cursor_next<kSparse, kMode>(p, nxt, it1);
       if (have_next) fetch_indices(nxt);  // in flight while this tile streams
       for (int c = 0; c < kNumChunks; ++c) {
         ok = __all_sync(0xffffffffu, wait_bounded(bar_k_empty + 8 * kst, kph ^ 1u, ctl));
@@ -581,50 +618,129 @@ __global__ void __launch_bounds__(kThreads, 1)
       const MmaCtx m{sK, sQ, q_chunk_bytes, bar_q_full, bar_q_empty, bar_k_full, bar_k_empty,
                      bar_acc_full, bar_acc_empty, tmem_base, it0, it1};
       if (warp == kMmaWarpA)
-        mma_issue<kSparse, 0>(p, m, ctl);
+        mma_issue<kSparse, kMode, 0>(p, m, ctl);
       else
-        mma_issue<kSparse, 1>(p, m, ctl);
+        mma_issue<kSparse, kMode, 1>(p, m, ctl);
       // All MMAs this thread issued must be complete before TMEM is released.
       umma_commit(bar_teardown);
       wait_drain(bar_teardown, 0, 200000000);
     }
     __syncwarp();
-  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4 * kEpiGroups) {
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ============================================================ epilogue
-    const int wg = (warp - kEpiWarp0) >> 2;  // epilogue warpgroup
     const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-    const int et = quarter * 32 + lane;      // key slot inside the tile
-    float* L = ltab + wg * kMaxN;
-    const int bar_id = 1 + wg;
+    const int et = quarter * 32 + lane;      // TMEM lane: key slot (L1 pass) or q row (LSE pass)
+    float* L = ltab;
+    constexpr int bar_id = 1;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t acc = 0;
-    int table_item = -1;
     bool ok = true;
     const float c2 = p.c_log2;
+    const float neg_inf = __int_as_float(0xff800000);
+    const float pos_inf = __int_as_float(0x7f800000);
     for (int it = it0; it < it1 && ok; ++it) {
       const WorkItem w = p.items[it];
       int tl;
       const int nt = item_tiles<kSparse>(p, w, tl);
-      for (int t = 0; t < nt; ++t, ++acc) {
-        if (static_cast<int>(acc % kEpiGroups) != wg) continue;
-        if (table_item != it) {
-          // lse * log2(e) per accumulator column; +inf beyond the real heads
-          // so that padded columns contribute exp2(-inf) = 0.
-          wg_sync(bar_id);
-          if (et < p.n_mma) {
-            float v = __int_as_float(0x7f800000);
-            if (et < w.nrows * p.G) v = __ldg(p.lse + static_cast<int64_t>(w.q_tok) * p.G + et) * kLog2e;
-            L[et] = v;
+      const EffLen e = effective_lengths(p, w);
+      if (kMode != kModeL1) {
+        // ---------------------------------------------------- LSE pass
+        // Thread et owns accumulator row et: head et % G of token
+        // q_tok + et / G.  It keeps a running maximum m and sum of
+        // exp2(x - m) over the kept slots, x = s * scale * log2(e), so that
+        // log2 sum_i exp2(x_i) = m + log2(sum).
+        int limit = 0;  // dense form: this row sees keys j < limit
+        if (!kSparse) {
+          const int r = et / p.G;
+          if (r < min(w.nrows, e.Sq - w.r0)) {
+            limit = e.Sk;
+            if (p.mask_mode != 0) limit = min(e.Sk, max(0, w.r0 + r + e.Sk - e.Sq + 1));
+            limit = min(limit, p.width);
           }
-          wg_sync(bar_id);
-          table_item = it;
         }
+        float m = neg_inf, sum = 0.f;
+        for (int t = 0; t < nt; ++t, ++acc) {
+          const uint32_t buf = acc & (kAccBufs - 1);
+          const uint32_t mset = (acc & 1u) * 4;
+          if (kSparse) {
+            // the slot masks are shared: each warp publishes its 32 slots
+            const int slot = t * kTileKeys + et;
+            bool valid = false;
+            if (slot < tl) {
+              const int j = __ldg(p.idx + static_cast<int64_t>(w.q_tok) * p.topk + slot);
+              valid = (j >= 0) && (j < e.Sk) && (p.mask_mode == 0 || j <= w.r0 + e.Sk - e.Sq);
+            }
+            const uint32_t bits = __ballot_sync(0xffffffffu, valid);
+            if (lane == 0) vmask[mset + quarter] = bits;
+          }
+          bool got = wait_bounded(bar_acc_full + 8 * buf, (acc / kAccBufs) & 1u, ctl);
+          got = wg_all(bar_id, got);  // a barrier: the slot masks are visible after it
+          if (!got) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + lane_addr + buf * kAccCols;
+          uint32_t words[4] = {0u, 0u, 0u, 0u};
+          if (kSparse) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) words[q4] = vmask[mset + q4];
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < kTileKeys; c0 += 16) {
+            float f[16], g[16];
+            tmem_ld16(taddr + c0, f);
+            tmem_ld16(taddr + kHalfCols + c0, g);
+            const uint32_t bits16 = kSparse ? (words[c0 >> 5] >> (c0 & 16)) : 0u;
+            float cm = neg_inf;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const bool keep = kSparse ? ((bits16 >> k) & 1u) != 0 : (t * kTileKeys + c0 + k < limit);
+              f[k] = keep ? (f[k] + g[k]) * c2 : neg_inf;
+              cm = fmaxf(cm, f[k]);
+            }
+            if (cm > m) {
+              sum *= fast_exp2(m - cm);  // exp2(-inf) = 0 on the first kept slot
+              m = cm;
+            }
+            if (m != neg_inf) {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) sum += fast_exp2(f[k] - m);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(bar_acc_empty + 8 * buf);
+        }
+        if (!ok) break;
+        const float lse2 = sum > 0.f ? m + log2f(sum) : neg_inf;  // -inf: no kept slot
+        if (et < w.nrows * p.G) p.lse_out[static_cast<int64_t>(w.q_tok) * p.G + et] = lse2 * kLn2;
+        if (kMode == kModeFused && nt > 0) {
+          // the L1 pass reads the LSE per accumulator column
+          wg_sync(bar_id);
+          if (et < p.n_mma) L[et] = et < w.nrows * p.G ? lse2 : pos_inf;
+          wg_sync(bar_id);
+        }
+      }
+      if (kMode == kModeLse) continue;
+      // ---------------------------------------------------- L1-norm pass
+      if (kMode == kModeL1 && nt > 0) {
+        // lse * log2(e) per accumulator column; +inf beyond the real heads
+        // so that padded columns contribute exp2(-inf) = 0.
+        wg_sync(bar_id);
+        if (et < p.n_mma) {
+          float v = pos_inf;
+          if (et < w.nrows * p.G) v = __ldg(p.lse + static_cast<int64_t>(w.q_tok) * p.G + et) * kLog2e;
+          L[et] = v;
+        }
+        wg_sync(bar_id);
+      }
+      for (int t = 0; t < nt; ++t, ++acc) {
         const int slot = t * kTileKeys + et;
         bool valid = false;
         if (kSparse) {
           if (slot < tl) {
             const int j = __ldg(p.idx + static_cast<int64_t>(w.q_tok) * p.topk + slot);
-            valid = (j >= 0) && (j < w.Sk) && (p.mask_mode == 0 || j <= w.r0 + w.Sk - w.Sq);
+            valid = (j >= 0) && (j < e.Sk) && (p.mask_mode == 0 || j <= w.r0 + e.Sk - e.Sq);
           }
         }
         const uint32_t buf = acc & (kAccBufs - 1);
@@ -667,8 +783,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               s += fast_exp2(fmaf(f[k] + g[k], c2, -L[c0 + k]));
               if (++g_in == p.G) {
                 if (r < w.nrows && j < p.width) {
-                  const bool v = (j < w.Sk) &&
-                                 (p.mask_mode == 0 || j <= w.r0 + r + w.Sk - w.Sq);
+                  const bool v = (j < e.Sk) && (w.r0 + r < e.Sq) &&
+                                 (p.mask_mode == 0 || j <= w.r0 + r + e.Sk - e.Sq);
                   p.out[static_cast<int64_t>(w.q_tok + r) * p.width + j] = v ? s * p.inv_g : 0.f;
                 }
                 s = 0.f;
@@ -683,15 +799,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // Slots past the last computed tile are zero.
-      if ((it - it0) % kEpiGroups == wg) {
-        if (kSparse) {
-          float* o = p.out + static_cast<int64_t>(w.q_tok) * p.topk;
-          for (int s = nt * kTileKeys + et; s < p.topk; s += kTileKeys) o[s] = 0.f;
-        } else {
-          for (int r = 0; r < w.nrows; ++r) {
-            float* o = p.out + static_cast<int64_t>(w.q_tok + r) * p.width;
-            for (int j = nt * kTileKeys + et; j < p.width; j += kTileKeys) o[j] = 0.f;
-          }
+      if (kSparse) {
+        float* o = p.out + static_cast<int64_t>(w.q_tok) * p.topk;
+        for (int s = nt * kTileKeys + et; s < p.topk; s += kTileKeys) o[s] = 0.f;
+      } else {
+        for (int r = 0; r < w.nrows; ++r) {
+          float* o = p.out + static_cast<int64_t>(w.q_tok + r) * p.width;
+          for (int j = nt * kTileKeys + et; j < p.width; j += kTileKeys) o[j] = 0.f;
         }
       }
     }
@@ -729,19 +843,32 @@ __global__ void smla_wait_timeout_probe_kernel(int32_t* status, int64_t timeout_
 }
 
 cudaError_t configure_fused(int smem_bytes) {
-  cudaError_t e = cudaFuncSetAttribute(smla_fused_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(smla_fused_kernel<false>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  const void* fns[] = {
+      reinterpret_cast<const void*>(smla_fused_kernel<true, kModeL1>),
+      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeL1>),
+      reinterpret_cast<const void*>(smla_fused_kernel<true, kModeLse>),
+      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeLse>),
+      reinterpret_cast<const void*>(smla_fused_kernel<true, kModeFused>),
+      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeFused>)};
+  for (const void* f : fns) {
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
-cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int grid,
+cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int mode, int grid,
                          int smem_bytes, cudaStream_t stream) {
-  if (sparse)
-    smla_fused_kernel<true><<<grid, kThreads, smem_bytes, stream>>>(p, tmap_q);
-  else
-    smla_fused_kernel<false><<<grid, kThreads, smem_bytes, stream>>>(p, tmap_q);
+  const dim3 g(grid), b(kThreads);
+  switch (mode * 2 + (sparse ? 1 : 0)) {
+    case kModeL1 * 2 + 1: smla_fused_kernel<true, kModeL1><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeL1 * 2: smla_fused_kernel<false, kModeL1><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeLse * 2 + 1: smla_fused_kernel<true, kModeLse><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeLse * 2: smla_fused_kernel<false, kModeLse><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeFused * 2 + 1: smla_fused_kernel<true, kModeFused><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeFused * 2: smla_fused_kernel<false, kModeFused><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

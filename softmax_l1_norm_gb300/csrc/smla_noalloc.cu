@@ -144,7 +144,7 @@ void fill_items(const smla_l1norm_desc* d, const Shape& s) {
       g_items_in_order[n++] = WorkItem{static_cast<int32_t>(q0 + r0), static_cast<int32_t>(nrows),
                                        static_cast<int32_t>(r0), static_cast<int32_t>(k0),
                                        static_cast<int32_t>(Sq), static_cast<int32_t>(Sk),
-                                       static_cast<int32_t>(tiles), 0};
+                                       static_cast<int32_t>(tiles), b};
     }
   }
 }
@@ -272,7 +272,7 @@ extern "C" smla_status smla_l1norm_run_noalloc(const smla_l1norm_desc* desc, con
   p.inv_g = 1.0f / static_cast<float>(s.G);
   p.timeout_ns = 2000LL * 1000000LL;
   e = smla::configure_fused(smem);
-  if (e == cudaSuccess) e = smla::launch_fused(p, tq, s.sparse, ctas, smem, cstream);
+  if (e == cudaSuccess) e = smla::launch_fused(p, tq, s.sparse, smla::kModeL1, ctas, smem, cstream);
   if (e != cudaSuccess) return fail_cuda(e);
   return SMLA_OK;
 }

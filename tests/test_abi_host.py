@@ -84,6 +84,7 @@ def test_layout_mismatch_and_null_desc():
     d.layout_k = 0
     assert lib.smla_l1norm_plan_create(ctypes.byref(d), None) == smla.SMLA_ERR_NULLPTR
     assert lib.smla_l1norm_run(None, None, None, None, None, None, None, None) == smla.SMLA_ERR_NULLPTR
+    assert lib.smla_l1norm_run_tensors(None, None, None) == smla.SMLA_ERR_NULLPTR
 
 
 def _tokens_of(items):
@@ -113,6 +114,13 @@ def test_schedule_covers_every_token_once(G, topk, mask, layout):
     assert all(a <= b for a, b in zip(offs, offs[1:]))
     toks = _tokens_of(items)
     assert sorted(toks) == list(range(n_tok))
+    # the last field is the item's sequence number (it indexes seqused_q / seqused_k)
+    if layout == "TND":
+        for it in items:
+            b = it[7]
+            assert cu[b] <= it[0] < cu[b + 1] and it[3] == cu[b]
+    else:
+        assert all(it[7] == it[0] // 700 for it in items)
     if topk > 0:
         assert info.rows_per_item == 1 and info.mma_n == max(16, -(-G // 16) * 16)
     else:

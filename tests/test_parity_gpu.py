@@ -196,3 +196,73 @@ def test_config4_varlen_tnd_full_size_sampled(lib):
 
 def test_config5_long_clustered_full_size_sampled(lib):
     sampled_parity(lib, 5, n_sample=16)
+
+
+# ---------------------------------------------------------------- seqused_q / seqused_k
+def seqused_parity(lib, w, su_q, su_k):
+    """Parity with per-sequence participating lengths.  The LSE is the exact
+    forward LSE over the cut problem, so every row with a kept slot sums to
+    1; rows past seqused_q and slots past seqused_k are exactly 0."""
+    kw = oracle_kwargs(w)
+    kw.update(seqused_q=su_q, seqused_k=su_k)
+    W.set_lse_rows(w, oracle.softmax_lse(w.q_bits, w.k_bits, **kw).astype(np.float32))
+    want = oracle.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **kw)
+    plan = lib.Plan(**plan_kwargs(w))
+    t = to_device(w)
+    dev = lambda v: None if v is None else torch.tensor(np.asarray(v, np.int32), device="cuda")
+    out = plan.run(t["q"], t["k"], t["lse"], sparse_indices=t["idx"], topk_length=t["tl"],
+                   seqused_q=dev(su_q), seqused_k=dev(su_k))
+    torch.cuda.synchronize()
+    code, _ = plan.status()
+    assert code == lib.SMLA_OK
+    got = out.cpu().numpy()
+    assert_close(got, want, what=w.name)
+    rows = got.reshape(w.n_tokens, -1).astype(np.float64)
+    assert np.all(rows[want.reshape(w.n_tokens, -1) == 0.0] == 0.0), "cut slots must be exactly 0"
+    has = ~np.isneginf(w.lse_rows()[:, 0])
+    assert np.all(np.abs(rows[has].sum(axis=1) - 1.0) <= ROWSUM_TOL)
+    assert np.all(rows[~has] == 0.0)
+    return got
+
+
+def test_seqused_sparse_bsnd(lib):
+    w = W.make_workload(name="seqused_sparse", layout="BSND", dtype="bf16", B=3, S1=40, S2=600, G=16,
+                        topk=300, mask_mode=3, seed=3100, lse=None)
+    got = seqused_parity(lib, w, su_q=[40, 17, 0], su_k=[600, 250, 5])
+    g = got.reshape(3, 40, -1)
+    assert np.all(g[1, 17:] == 0.0) and np.all(g[2] == 0.0)
+
+
+def test_seqused_sparse_tnd_keys_only_and_negative(lib):
+    w = W.make_workload(name="seqused_sparse_tnd", layout="TND", dtype="fp16", seqlens_q=[130, 1, 77],
+                        seqlens_k=[130, 5, 300], G=64, topk=256, mask_mode=0, seed=3101, lse=None)
+    seqused_parity(lib, w, su_q=None, su_k=[-4, 9, 129])
+
+
+def test_seqused_dense_tnd(lib):
+    w = W.make_workload(name="seqused_dense_tnd", layout="TND", dtype="bf16", seqlens_q=[70, 9, 130],
+                        seqlens_k=[90, 9, 200], G=16, topk=0, mask_mode=3, max_seqlen_k=220,
+                        seed=3102, lse=None)
+    seqused_parity(lib, w, su_q=[50, 9, 3], su_k=[1000, 0, 77])
+
+
+def test_seqused_dense_shorter_queries_see_more_keys(lib):
+    """Cutting Sq moves the right-down causal diagonal: with Sq' = 20 and
+    Sk = 64, row 0 sees keys 0..44."""
+    w = W.make_workload(name="seqused_diag", layout="BSND", dtype="fp16", B=1, S1=64, S2=64, G=8,
+                        topk=0, mask_mode=3, seed=3103, lse=None)
+    got = seqused_parity(lib, w, su_q=[20], su_k=None).reshape(64, 64)
+    nz = (got != 0.0).sum(axis=1)
+    assert nz[0] == 45 and nz[19] == 64 and np.all(nz[20:] == 0)
+
+
+def test_seqused_full_lengths_bitwise_equal_to_run(lib):
+    w = W.make_workload(layout="BSND", dtype="bf16", B=2, S1=33, S2=700, G=128, topk=512,
+                        mask_mode=3, seed=3104)
+    a, plan, t, _ = run_gpu(lib, w)
+    full = torch.tensor([33, 33], dtype=torch.int32, device="cuda")
+    fullk = torch.tensor([700, 700], dtype=torch.int32, device="cuda")
+    b = plan.run(t["q"], t["k"], t["lse"], sparse_indices=t["idx"], topk_length=t["tl"],
+                 seqused_q=full, seqused_k=fullk)
+    torch.cuda.synchronize()
+    assert np.array_equal(a.view(np.uint32), b.cpu().numpy().view(np.uint32))
