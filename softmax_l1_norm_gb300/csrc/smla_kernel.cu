@@ -227,6 +227,32 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&f)[16]) {
   for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
 }
 
+// Split form for software pipelining: issue the loads of the next 16
+// columns of both accumulator halves, work on the current ones, then wait.
+// The wait names the in-flight registers so that no use of them moves
+// above it.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+      " [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]),
+                 "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]),
+                 "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15])
+               :
+               : "memory");
+  asm volatile(""
+               : "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]),
+                 "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]),
+                 "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -659,19 +685,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         float m = neg_inf, sum = 0.f;
+        // sparse form: this thread's slot index, loaded one tile ahead
+        const int32_t* idx_row = kSparse ? p.idx + static_cast<int64_t>(w.q_tok) * p.topk : nullptr;
+        int j_next = (kSparse && nt > 0 && et < tl) ? __ldg(idx_row + et) : -1;
         for (int t = 0; t < nt; ++t, ++acc) {
           const uint32_t buf = acc & (kAccBufs - 1);
           const uint32_t mset = (acc & 1u) * 4;
           if (kSparse) {
             // the slot masks are shared: each warp publishes its 32 slots
             const int slot = t * kTileKeys + et;
-            bool valid = false;
-            if (slot < tl) {
-              const int j = __ldg(p.idx + static_cast<int64_t>(w.q_tok) * p.topk + slot);
-              valid = (j >= 0) && (j < e.Sk) && (p.mask_mode == 0 || j <= w.r0 + e.Sk - e.Sq);
-            }
+            const int j = j_next;
+            const bool valid = (slot < tl) && (j >= 0) && (j < e.Sk) &&
+                               (p.mask_mode == 0 || j <= w.r0 + e.Sk - e.Sq);
             const uint32_t bits = __ballot_sync(0xffffffffu, valid);
             if (lane == 0) vmask[mset + quarter] = bits;
+            j_next = (slot + kTileKeys < tl) ? __ldg(idx_row + slot + kTileKeys) : -1;
           }
           bool got = wait_bounded(bar_acc_full + 8 * buf, (acc / kAccBufs) & 1u, ctl);
           got = wg_all(bar_id, got);  // a barrier: the slot masks are visible after it
@@ -681,32 +709,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t taddr = tmem_base + lane_addr + buf * kAccCols;
-          uint32_t words[4] = {0u, 0u, 0u, 0u};
-          if (kSparse) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) words[q4] = vmask[mset + q4];
-          }
-#pragma unroll
-          for (int c0 = 0; c0 < kTileKeys; c0 += 16) {
-            float f[16], g[16];
-            tmem_ld16(taddr + c0, f);
-            tmem_ld16(taddr + kHalfCols + c0, g);
-            const uint32_t bits16 = kSparse ? (words[c0 >> 5] >> (c0 & 16)) : 0u;
-            float cm = neg_inf;
+          // 16 columns at a time: x = keep ? s * scale * log2(e) : -inf;
+          // the running maximum moves once per 16 columns (tree maximum) and
+          // the sum is split over four chains.  The loop is kept rolled: the
+          // warps of all roles share the instruction cache.
+          const int lim = limit - t * kTileKeys;  // dense form: columns c < lim are kept
+          auto lse16 = [&](const uint32_t (&fa)[16], const uint32_t (&ga)[16], int c0, uint32_t bits16) {
+            float x[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              const bool keep = kSparse ? ((bits16 >> k) & 1u) != 0 : (t * kTileKeys + c0 + k < limit);
-              f[k] = keep ? (f[k] + g[k]) * c2 : neg_inf;
-              cm = fmaxf(cm, f[k]);
+              const bool keep = kSparse ? ((bits16 >> k) & 1u) != 0 : (c0 + k < lim);
+              x[k] = keep ? (__uint_as_float(fa[k]) + __uint_as_float(ga[k])) * c2 : neg_inf;
             }
+            float t8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t8[k] = fmaxf(x[k], x[k + 8]);
+            const float cm = fmaxf(fmaxf(fmaxf(t8[0], t8[4]), fmaxf(t8[1], t8[5])),
+                                   fmaxf(fmaxf(t8[2], t8[6]), fmaxf(t8[3], t8[7])));
             if (cm > m) {
               sum *= fast_exp2(m - cm);  // exp2(-inf) = 0 on the first kept slot
               m = cm;
             }
             if (m != neg_inf) {
+              float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-              for (int k = 0; k < 16; ++k) sum += fast_exp2(f[k] - m);
+              for (int k = 0; k < 16; ++k) s4[k & 3] += fast_exp2(x[k] - m);
+              sum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             }
+          };
+          uint32_t fa[16], ga[16], fb[16], gb[16];
+          tmem_ld16_issue(taddr, fa);
+          tmem_ld16_issue(taddr + kHalfCols, ga);
+          tmem_ld_wait(fa, ga);
+#pragma unroll 1
+          for (int c0 = 0; c0 < kTileKeys; c0 += 32) {
+            tmem_ld16_issue(taddr + c0 + 16, fb);
+            tmem_ld16_issue(taddr + kHalfCols + c0 + 16, gb);
+            const uint32_t w32 = kSparse ? vmask[mset + (c0 >> 5)] : 0u;
+            lse16(fa, ga, c0, w32 & 0xffffu);
+            tmem_ld_wait(fb, gb);
+            if (c0 + 32 < kTileKeys) {
+              tmem_ld16_issue(taddr + c0 + 32, fa);
+              tmem_ld16_issue(taddr + kHalfCols + c0 + 32, ga);
+            }
+            lse16(fb, gb, c0 + 16, w32 >> 16);
+            if (c0 + 32 < kTileKeys) tmem_ld_wait(fa, ga);
           }
           tc_fence_before();
           mbar_arrive(bar_acc_empty + 8 * buf);
@@ -754,16 +801,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_addr + buf * kAccCols;
         if (kSparse) {
+          // sum over the heads of exp2(s * scale * log2(e) - lse * log2(e)),
+          // 16 columns at a time, the next 16 loading meanwhile
           float s0 = 0.f, s1 = 0.f;
-          for (int c0 = 0; c0 < p.n_mma; c0 += 16) {
-            float f[16], g[16];
-            tmem_ld16(taddr + c0, f);
-            tmem_ld16(taddr + kHalfCols + c0, g);
+          auto l1_16 = [&](const uint32_t (&fa)[16], const uint32_t (&ga)[16], int c0) {
 #pragma unroll
             for (int k = 0; k < 16; k += 2) {
-              s0 += fast_exp2(fmaf(f[k] + g[k], c2, -L[c0 + k]));
-              s1 += fast_exp2(fmaf(f[k + 1] + g[k + 1], c2, -L[c0 + k + 1]));
+              s0 += fast_exp2(fmaf(__uint_as_float(fa[k]) + __uint_as_float(ga[k]), c2, -L[c0 + k]));
+              s1 += fast_exp2(fmaf(__uint_as_float(fa[k + 1]) + __uint_as_float(ga[k + 1]), c2, -L[c0 + k + 1]));
             }
+          };
+          const int n = p.n_mma;  // a multiple of 16
+          uint32_t fa[16], ga[16], fb[16], gb[16];
+          tmem_ld16_issue(taddr, fa);
+          tmem_ld16_issue(taddr + kHalfCols, ga);
+          tmem_ld_wait(fa, ga);
+          for (int c0 = 0; c0 < n; c0 += 32) {
+            const bool has_b = c0 + 16 < n;
+            const bool has_a = c0 + 32 < n;
+            if (has_b) {
+              tmem_ld16_issue(taddr + c0 + 16, fb);
+              tmem_ld16_issue(taddr + kHalfCols + c0 + 16, gb);
+            }
+            l1_16(fa, ga, c0);
+            if (has_b) tmem_ld_wait(fb, gb);
+            if (has_a) {
+              tmem_ld16_issue(taddr + c0 + 32, fa);
+              tmem_ld16_issue(taddr + kHalfCols + c0 + 32, ga);
+            }
+            if (has_b) l1_16(fb, gb, c0 + 16);
+            if (has_a) tmem_ld_wait(fa, ga);
           }
           tc_fence_before();
           mbar_arrive(bar_acc_empty + 8 * buf);
