@@ -425,8 +425,11 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
       }
       // The barrier test for the next stage is issued before the current
       // stage's MMAs so that its latency overlaps them; only a stage that is
-      // not ready yet costs a blocking wait.
+      // not ready yet costs a blocking wait.  A stage already acquired by
+      // that test before a proxy fence is covered by the fence and needs
+      // none of its own (with copies in flight a fence waits for all of them).
       bool ready = mbar_test_wait(m.bar_k_full + 8 * sl[H], ph[H]);
+      bool covered = false;
 #pragma unroll
       for (int c = H; c < kNumChunks; c += 2) {
         if (!ready) {
@@ -441,7 +444,8 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
         const bool ready_next = (c + 2 < kNumChunks) ? mbar_test_wait(m.bar_k_full + 8 * sl[c + 2], ph[c + 2]) : false;
         // the producers' cp.async writes (generic proxy), acquired through
         // the barrier, become visible to the tensor cores (async proxy)
-        fence_proxy_async();
+        if (!covered) fence_proxy_async();
+        covered = ready_next;
         tc_fence_after();
         const uint32_t k_lo = k_lo0 + sl[c] * (kKStageBytes >> 4);
         const uint32_t q_lo = q_lo0 + c * b_step;
