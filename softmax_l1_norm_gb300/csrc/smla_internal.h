@@ -25,7 +25,7 @@ constexpr int kAccBufs = 2;
 constexpr int kAccCols = 256;
 constexpr int kHalfCols = 128;
 constexpr int kMaxN = 128;  // largest MMA N (R*G padded to 16)
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 constexpr int kThreads = 384;  // 12 warps: 2 MMA issuers, 4 key producers, one epilogue warpgroup, q loader, 1 spare
 
 // Status word bits.
