@@ -139,6 +139,9 @@ typedef struct {
   double mean_cta_cost;    /* average CTA                                        */
   int64_t q_rows_total;    /* rows of the 2-D view of q (tokens * G)             */
   int64_t k_rows_total;    /* rows of the 2-D view of k (B*S2 or T2)             */
+  int32_t host_chunks;     /* token chunks smla_l1norm_run_from_host pipelines
+                              (copies of one chunk overlap the kernel of the
+                              previous one); 0 = one copy, one kernel, one copy */
 } smla_plan_info;
 
 /*
@@ -263,12 +266,22 @@ typedef struct {
 smla_status smla_l1norm_io_sizes(const smla_plan *plan, smla_io_sizes *sizes);
 
 /*
- * End-to-end form for callers whose tensors live in HOST memory: on
- * ``stream``, copy each host input into the caller's device buffer of the
- * same role (cudaMemcpyAsync, one copy per tensor), run, and copy the output
- * back to ``h_out``.  Host buffers should be page-locked for the copies to be
- * asynchronous.  Pass NULL for tensors the plan does not use.  Returns as
- * run(); the host output is valid after the stream is synchronised.
+ * End-to-end form for callers whose tensors live in HOST memory: copy each
+ * host input into the caller's device buffer of the same role, run, and copy
+ * the output back to ``h_out``.  Host buffers should be page-locked for the
+ * copies to be asynchronous.  Pass NULL for tensors the plan does not use.
+ * Returns as run(); the host output is valid after ``stream`` is
+ * synchronised.
+ *
+ * When the plan has host_chunks > 0 the call is pipelined over token
+ * chunks: the plan's own copy-in stream moves k, then each chunk's rows of
+ * q, lse, indices and topk_length; ``stream`` runs each chunk's kernel as
+ * soon as its rows have landed; the plan's copy-out stream returns each
+ * chunk's output rows as soon as its kernel is done.  Both plan streams
+ * start after the work already queued on ``stream``, and ``stream`` waits
+ * for the last copy, so to the caller the call is ordered on ``stream`` like
+ * any other.  Otherwise (small problems) it is one copy per tensor, one
+ * kernel and one copy back, all on ``stream``.
  */
 smla_status smla_l1norm_run_from_host(const smla_plan *plan,
                                       const void *h_q, const void *h_k, const float *h_lse,

@@ -144,7 +144,8 @@ struct Schedule {
 // Any assignment gives the same output bits; the schedule only balances
 // time.  Cost of an item: its 128-key tiles, plus a per-token overhead for
 // the q load and the zero tail.
-Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ctas) {
+Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ctas, int64_t tok_lo = 0,
+                        int64_t tok_hi = INT64_MAX) {
   Schedule s;
   std::vector<WorkItem> items;
   std::vector<double> cost;
@@ -154,6 +155,7 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
     if (g.sparse) {
       for (int64_t r = 0; r < Sq; ++r) {
         const int64_t tok = g.q0[b] + r;
+        if (tok < tok_lo || tok >= tok_hi) continue;
         int64_t n;
         if (d->topk_length_hint != nullptr) {
           n = std::min<int64_t>(std::max<int32_t>(d->topk_length_hint[tok], 0), d->topk);
@@ -173,6 +175,7 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
       }
     } else {
       for (int64_t r0 = 0; r0 < Sq; r0 += g.R) {
+        if (g.q0[b] + r0 < tok_lo || g.q0[b] + r0 >= tok_hi) continue;
         const int64_t nrows = std::min<int64_t>(g.R, Sq - r0);
         const int64_t vis = visible_keys(r0 + nrows - 1, Sq, Sk, d->mask_mode);
         const int64_t tiles = ceil_div(std::min<int64_t>(vis, g.width), smla::kTileKeys);
@@ -318,7 +321,28 @@ struct smla_plan {
   WorkItem* d_items = nullptr;
   smla_plan_info info{};
   int64_t timeout_ns = 0;
+  // run_from_host pipeline: token chunks, each with its own work schedule,
+  // so that the copies of one chunk overlap the kernel of the previous one
+  std::vector<int64_t> chunk_lo, chunk_hi;
+  std::vector<int32_t*> d_chunk_begin;
+  std::vector<WorkItem*> d_chunk_items;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  std::vector<cudaEvent_t> events;  // start, end, then per chunk: inputs landed, kernel done
 };
+
+namespace {
+
+constexpr int kHostChunks = 4;
+
+void release_plan(smla_plan* plan) {
+  for (cudaEvent_t e : plan->events) cudaEventDestroy(e);
+  if (plan->s_in != nullptr) cudaStreamDestroy(plan->s_in);
+  if (plan->s_out != nullptr) cudaStreamDestroy(plan->s_out);
+  if (plan->dbuf != nullptr) cudaFree(plan->dbuf);
+  delete plan;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -359,14 +383,14 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
 
   cudaError_t e = cudaGetDevice(&plan->device);
   if (e != cudaSuccess) {
-    delete plan;
+    release_plan(plan);
     return cuda_fail(e, "cudaGetDevice");
   }
   int sms = 0, optin = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, plan->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, plan->device);
   if (e != cudaSuccess) {
-    delete plan;
+    release_plan(plan);
     return cuda_fail(e, "cudaDeviceGetAttribute");
   }
   int ctas = desc->num_ctas > 0 ? desc->num_ctas : sms;
@@ -375,35 +399,83 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   plan->stages = stages_for(g.n_mma, optin);
   plan->smem = smla::smem_bytes_for(g.n_mma, plan->stages);
   if (plan->smem > optin) {
-    delete plan;
+    release_plan(plan);
     return SMLA_ERR_INVALID;
   }
   const Schedule s = build_schedule(desc, g, ctas);
   fill_info(g, s, ctas, plan->stages, plan->smem, &plan->info);
 
-  // one device buffer: status word | CTA offsets | work items
+  // Token chunks for run_from_host: cut the token-ordered work items into
+  // kHostChunks runs of about equal token count (an item never straddles a
+  // cut), when there is enough work for every CTA in each chunk.
+  std::vector<Schedule> cs;
+  if (static_cast<int64_t>(s.items.size()) >= static_cast<int64_t>(kHostChunks) * ctas * 2) {
+    std::vector<WorkItem> ordered = s.items;
+    std::sort(ordered.begin(), ordered.end(), [](const WorkItem& a, const WorkItem& b) { return a.q_tok < b.q_tok; });
+    int64_t cut = 0;
+    plan->chunk_lo.push_back(0);
+    for (const WorkItem& w : ordered) {
+      const int next_chunk = static_cast<int>(plan->chunk_lo.size());
+      if (next_chunk < kHostChunks && w.q_tok >= g.n_tokens * next_chunk / kHostChunks && w.q_tok > cut) {
+        plan->chunk_hi.push_back(w.q_tok);
+        plan->chunk_lo.push_back(w.q_tok);
+        cut = w.q_tok;
+      }
+    }
+    plan->chunk_hi.push_back(g.n_tokens);
+    for (size_t c = 0; c < plan->chunk_lo.size(); ++c)
+      cs.push_back(build_schedule(desc, g, ctas, plan->chunk_lo[c], plan->chunk_hi[c]));
+  }
+
+  // one device buffer: status word | CTA offsets | work items | per chunk: CTA offsets | work items
+  auto round256 = [](size_t n) { return ((n + 255) / 256) * 256; };
   const size_t off_begin = 256;
-  const size_t off_items = off_begin + ((s.cta_begin.size() * sizeof(int32_t) + 255) / 256) * 256;
-  const size_t bytes = off_items + std::max<size_t>(1, s.items.size()) * sizeof(WorkItem);
+  const size_t off_items = off_begin + round256(s.cta_begin.size() * sizeof(int32_t));
+  size_t bytes = off_items + round256(std::max<size_t>(1, s.items.size()) * sizeof(WorkItem));
+  std::vector<size_t> off_cb, off_ci;
+  for (const Schedule& c : cs) {
+    off_cb.push_back(bytes);
+    bytes += round256(c.cta_begin.size() * sizeof(int32_t));
+    off_ci.push_back(bytes);
+    bytes += round256(std::max<size_t>(1, c.items.size()) * sizeof(WorkItem));
+  }
   e = cudaMalloc(&plan->dbuf, bytes);
   if (e != cudaSuccess) {
-    delete plan;
+    release_plan(plan);
     return cuda_fail(e, "cudaMalloc(plan)");
   }
   std::vector<uint8_t> host(bytes, 0);
   std::memcpy(host.data() + off_begin, s.cta_begin.data(), s.cta_begin.size() * sizeof(int32_t));
   if (!s.items.empty()) std::memcpy(host.data() + off_items, s.items.data(), s.items.size() * sizeof(WorkItem));
+  for (size_t c = 0; c < cs.size(); ++c) {
+    std::memcpy(host.data() + off_cb[c], cs[c].cta_begin.data(), cs[c].cta_begin.size() * sizeof(int32_t));
+    if (!cs[c].items.empty())
+      std::memcpy(host.data() + off_ci[c], cs[c].items.data(), cs[c].items.size() * sizeof(WorkItem));
+  }
   e = cudaMemcpy(plan->dbuf, host.data(), bytes, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = smla::configure_fused(plan->smem);
+  if (e == cudaSuccess && !cs.empty()) {
+    e = cudaStreamCreateWithFlags(&plan->s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking);
+    for (size_t i = 0; e == cudaSuccess && i < 2 + 2 * cs.size(); ++i) {
+      cudaEvent_t ev = nullptr;
+      e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+      if (e == cudaSuccess) plan->events.push_back(ev);
+    }
+  }
   if (e != cudaSuccess) {
-    cudaFree(plan->dbuf);
-    delete plan;
+    release_plan(plan);
     return cuda_fail(e, "plan upload");
   }
   auto* b = static_cast<uint8_t*>(plan->dbuf);
   plan->d_status = reinterpret_cast<int32_t*>(b);
   plan->d_cta_begin = reinterpret_cast<int32_t*>(b + off_begin);
   plan->d_items = reinterpret_cast<WorkItem*>(b + off_items);
+  plan->info.host_chunks = static_cast<int32_t>(cs.size());
+  for (size_t c = 0; c < cs.size(); ++c) {
+    plan->d_chunk_begin.push_back(reinterpret_cast<int32_t*>(b + off_cb[c]));
+    plan->d_chunk_items.push_back(reinterpret_cast<WorkItem*>(b + off_ci[c]));
+  }
   if (std::getenv("SMLA_LOG") != nullptr) {
     std::fprintf(stderr,
                  "[smla] plan: tokens=%lld items=%lld ctas=%d R=%d N=%d stages=%d smem=%d tiles=%lld "
@@ -418,8 +490,7 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
 
 void smla_l1norm_plan_destroy(smla_plan* plan) {
   if (plan == nullptr) return;
-  if (plan->dbuf != nullptr) cudaFree(plan->dbuf);
-  delete plan;
+  release_plan(plan);
 }
 
 smla_status smla_l1norm_output_shape(const smla_plan* plan, int64_t dims[4], int32_t* ndim) {
@@ -467,7 +538,7 @@ namespace {
 // t->softmax_lse and writes t->out; kModeLse writes lse_out only; kModeFused
 // writes lse_out and t->out.
 smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, float* lse_out, int mode,
-                        smla_stream_t stream) {
+                        smla_stream_t stream, int chunk = -1) {
   if (plan == nullptr || t == nullptr) return SMLA_ERR_NULLPTR;
   const Geometry& g = plan->geo;
   if (g.n_tokens == 0) return SMLA_OK;                       // empty q: nothing to do
@@ -495,8 +566,8 @@ smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, flo
   }
   smla::KernelParams p{};
   p.k = static_cast<const uint8_t*>(t->k);  // unread when there is no key row (every item has zero tiles)
-  p.items = plan->d_items;
-  p.cta_begin = plan->d_cta_begin;
+  p.items = chunk < 0 ? plan->d_items : plan->d_chunk_items[chunk];
+  p.cta_begin = chunk < 0 ? plan->d_cta_begin : plan->d_chunk_begin[chunk];
   p.status = plan->d_status;
   p.lse = wants_lse_in ? t->softmax_lse : nullptr;
   p.idx = g.sparse ? t->sparse_indices : nullptr;
@@ -571,17 +642,67 @@ smla_status smla_l1norm_run_from_host(const smla_plan* plan, const void* h_q, co
     if (c.n == 0) continue;
     if (c.dst == nullptr || c.src == nullptr) return SMLA_ERR_NULLPTR;
   }
-  for (const Copy& c : copies) {
-    if (c.n == 0) continue;
-    cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(H2D)");
+  const size_t n_chunks = plan->chunk_lo.size();
+  if (n_chunks == 0 || plan->geo.n_tokens == 0) {
+    for (const Copy& c : copies) {
+      if (c.n == 0) continue;
+      cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(H2D)");
+    }
+    smla_status r = smla_l1norm_run(plan, d_q, d_k, d_lse, d_indices, d_topk_length, d_out, stream);
+    if (r != SMLA_OK) return r;
+    if (s.out_bytes > 0) {
+      cudaError_t e = cudaMemcpyAsync(h_out, d_out, s.out_bytes, cudaMemcpyDeviceToHost, st);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(D2H)");
+    }
+    return SMLA_OK;
   }
-  smla_status r = smla_l1norm_run(plan, d_q, d_k, d_lse, d_indices, d_topk_length, d_out, stream);
-  if (r != SMLA_OK) return r;
-  if (s.out_bytes > 0) {
-    cudaError_t e = cudaMemcpyAsync(h_out, d_out, s.out_bytes, cudaMemcpyDeviceToHost, st);
+  // Pipelined over token chunks: the copy-in stream moves K, then each
+  // chunk's rows of q, lse, indices and topk_length; the caller's stream
+  // runs each chunk's kernel once its inputs have landed; the copy-out
+  // stream returns each chunk's output rows as soon as its kernel is done.
+  // H2D and D2H use different copy engines, so the only serial part is the
+  // host-to-device traffic.  The caller's stream waits for the last copy.
+  const smla_l1norm_tensors t{d_q, d_k, d_lse, d_indices, d_topk_length, nullptr, nullptr, d_out};
+  if (t.q == nullptr || t.softmax_lse == nullptr || t.out == nullptr) return SMLA_ERR_NULLPTR;
+  const int64_t n_tok = plan->geo.n_tokens;
+  auto per_token = [n_tok](size_t total) { return total / static_cast<size_t>(n_tok); };
+  const Copy rows[4] = {{d_q, h_q, per_token(s.q_bytes)},
+                        {d_lse, h_lse, per_token(s.lse_bytes)},
+                        {d_indices, h_indices, per_token(s.indices_bytes)},
+                        {d_topk_length, h_topk_length, per_token(s.topk_length_bytes)}};
+  const size_t out_row = per_token(s.out_bytes);
+  cudaEvent_t ev_start = plan->events[0], ev_end = plan->events[1];
+  cudaError_t e = cudaEventRecord(ev_start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->s_in, ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->s_out, ev_start, 0);
+  if (e == cudaSuccess && s.k_bytes > 0) e = cudaMemcpyAsync(d_k, h_k, s.k_bytes, cudaMemcpyHostToDevice, plan->s_in);
+  if (e != cudaSuccess) return cuda_fail(e, "run_from_host set-up");
+  for (size_t c = 0; c < n_chunks; ++c) {
+    const size_t lo = static_cast<size_t>(plan->chunk_lo[c]), hi = static_cast<size_t>(plan->chunk_hi[c]);
+    cudaEvent_t ev_in = plan->events[2 + 2 * c], ev_done = plan->events[3 + 2 * c];
+    for (const Copy& r : rows) {
+      if (r.n == 0 || hi == lo) continue;
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(r.dst) + lo * r.n, static_cast<const uint8_t*>(r.src) + lo * r.n,
+                          (hi - lo) * r.n, cudaMemcpyHostToDevice, plan->s_in);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(H2D)");
+    }
+    e = cudaEventRecord(ev_in, plan->s_in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_in, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "run_from_host chunk");
+    const smla_status r = launch_mode(plan, &t, nullptr, smla::kModeL1, stream, static_cast<int>(c));
+    if (r != SMLA_OK) return r;
+    e = cudaEventRecord(ev_done, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->s_out, ev_done, 0);
+    if (e == cudaSuccess && out_row > 0 && hi > lo)
+      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(h_out) + lo * out_row,
+                          reinterpret_cast<const uint8_t*>(d_out) + lo * out_row, (hi - lo) * out_row,
+                          cudaMemcpyDeviceToHost, plan->s_out);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(D2H)");
   }
+  e = cudaEventRecord(ev_end, plan->s_out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_end, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "run_from_host end");
   return SMLA_OK;
 }
 

@@ -142,6 +142,32 @@ def test_run_from_host_matches_run(lib):
     assert np.array_equal(pin["out"].numpy(), a)
 
 
+@pytest.mark.parametrize("kind", ["sparse_bsnd", "dense_tnd"])
+def test_run_from_host_pipelined_matches_run(lib, kind):
+    """With 8 CTAs every workload below has enough items for the token-chunk
+    pipeline of run_from_host; its output equals run()'s bit for bit."""
+    if kind == "sparse_bsnd":
+        w = W.make_workload(layout="BSND", dtype="bf16", B=2, S1=100, S2=900, G=32, topk=512,
+                            mask_mode=3, seed=2850)
+    else:
+        w = W.make_workload(layout="TND", dtype="fp16", seqlens_q=[70, 130, 40], seqlens_k=[90, 130, 60],
+                            G=64, topk=0, mask_mode=3, seed=2851)
+    a, plan, t, _ = run_gpu(lib, w, num_ctas=8)
+    assert plan.info.host_chunks == 4
+    pin = {k: (None if v is None else v.cpu().pin_memory()) for k, v in
+           {"q": t["q"], "k": t["k"], "lse": t["lse"], "indices": t["idx"], "topk_length": t["tl"]}.items()}
+    pin["out"] = torch.full(plan.output_shape, float("nan"), dtype=torch.float32).pin_memory()
+    dev = {"q": torch.empty_like(t["q"]), "k": torch.empty_like(t["k"]), "lse": torch.empty_like(t["lse"]),
+           "indices": None if t["idx"] is None else torch.empty_like(t["idx"]),
+           "topk_length": None if t["tl"] is None else torch.empty_like(t["tl"]),
+           "out": torch.empty(plan.output_shape, dtype=torch.float32, device="cuda")}
+    for _ in range(2):  # twice: the second call reuses the plan's streams and events
+        plan.run_from_host(pin, dev)
+        torch.cuda.synchronize()
+        assert np.array_equal(pin["out"].numpy().view(np.uint32), a.view(np.uint32))
+        pin["out"].fill_(float("nan"))
+
+
 def test_functional_api_matches_plan(lib):
     w = W.make_workload(layout="TND", dtype="bf16", seqlens_q=[33, 70], seqlens_k=[33, 90], G=16,
                         topk=64, mask_mode=3, seed=2800)
