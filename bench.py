@@ -187,7 +187,7 @@ import numpy as np
 P = json.loads(sys.argv[1])
 sys.path.insert(0, P["root"])
 import workloads as W, oracle
-w = W.make_config(P["config"])
+w = W.make_config(P["config"], seq_len=P.get("seq_len"))
 kw = dict(dtype=w.dtype, sparse_indices=w.sparse_indices, topk_length=w.topk_length,
           cu_seqlens_q=w.cu_seqlens_q, cu_seqlens_k=w.cu_seqlens_k, softmax_scale=w.softmax_scale,
           max_seqlen_k=w.max_seqlen_k, mask_mode=w.mask_mode, layout=w.layout)
@@ -229,13 +229,13 @@ print(json.dumps(res))
 """
 
 
-def cpu_oracle_run(config, warmup, steps, step_seconds, threads, seed=0):
+def cpu_oracle_run(config, warmup, steps, step_seconds, threads, seed=0, seq_len=None):
     """Time the CPU oracle, as it stands, on bounded samples of the workload's
     rows: ``warmup`` single rows, then ``steps`` steps of about
     ``step_seconds`` each.  Runs in a child process so the BLAS thread count
     is fixed before numpy loads and no CUDA context is involved."""
     params = json.dumps({"root": ROOT, "config": config, "seed": seed, "warmup": max(1, warmup),
-                         "steps": steps, "step_seconds": step_seconds})
+                         "steps": steps, "step_seconds": step_seconds, "seq_len": seq_len})
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
         env[v] = str(threads)
@@ -254,6 +254,26 @@ def host_threads():
         return os.cpu_count() or 1
 
 
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: the
+    implementer and part numbers), or None."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return None
+    fields = {}
+    for line in info.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return f"Arm implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return None
+
+
 # ----------------------------------------------------------------------------
 def run_reference(args, world, rank):
     """The CPU oracle as the reference arm: each step runs it on a bounded
@@ -261,11 +281,13 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     threads = host_threads()
-    r = cpu_oracle_run(args.config, args.warmup, args.steps, args.ref_step_seconds, threads)
+    r = cpu_oracle_run(args.config, args.warmup, args.steps, args.ref_step_seconds, threads,
+                       seq_len=args.seq_len)
     rows = sum(s[0] for s in r["steps"])
     pairs = sum(s[1] for s in r["steps"])
     secs = sum(s[2] for s in r["steps"])
-    name = W.CONFIG_NAMES[args.config]
+    name = W.CONFIG_NAMES[args.config] if args.seq_len is None else \
+        W.make_config(args.config, seq_len=args.seq_len).name
     value = pairs / secs
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -274,6 +296,7 @@ def run_reference(args, world, rank):
         "data": "synthetic (seeded)",
         "config": {"workload": name, "note": "CPU fp64 oracle on a bounded random sample of rows per step"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "cpu": cpu_model(),
                          "sample": f"{rows} random rows of {name} over {args.steps} steps "
                                    f"(~{args.ref_step_seconds}s each)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -292,7 +315,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream(device)
 
-    w = W.make_config(args.config)
+    w = W.make_config(args.config, seq_len=args.seq_len)
     name = w.name
     pairs, flops, bytes_ = workload_numbers(w)
     alg_bytes = sum(bytes_.values())
@@ -360,6 +383,23 @@ def run_ours(args, world, rank, local):
     code, flags = plan.status(stream)
     if code != smla.SMLA_OK:
         raise RuntimeError(f"device status {code} flags {flags} in the timed region")
+
+    # ------------------------------------------------ back-to-back launches (warm L2), secondary
+    warm = None
+    if not args.no_warm:
+        n_warm = max(3, min(args.steps, 50))
+        ew0 = torch.cuda.Event(enable_timing=True)
+        ew1 = torch.cuda.Event(enable_timing=True)
+        step()
+        ew0.record(stream)
+        for _ in range(n_warm):
+            step()
+        ew1.record(stream)
+        torch.cuda.synchronize(device)
+        warm_s = all_max(ew0.elapsed_time(ew1) / 1000.0, world, device)
+        warm = {"ms_per_launch": 1000 * warm_s / n_warm, "launches": n_warm,
+                "value": world * pairs * n_warm / warm_s, "unit": UNIT,
+                "note": "back to back, no L2 flush between launches (outside the timed region)"}
 
     # ------------------------------------------------ end to end through the host API
     e2e = None
@@ -431,9 +471,9 @@ def run_ours(args, world, rank, local):
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         threads = host_threads()
-        r = cpu_oracle_run(args.config, 1, 1, args.cpu_seconds, threads)
+        r = cpu_oracle_run(args.config, 1, 1, args.cpu_seconds, threads, seq_len=args.seq_len)
         n_rows, c_pairs, c_secs = r["steps"][0]
-        cpu = {"value": c_pairs / c_secs, "unit": UNIT, "cores": threads, "kind": "oracle",
+        cpu = {"value": c_pairs / c_secs, "unit": UNIT, "cores": threads, "kind": "oracle", "cpu": cpu_model(),
                "sample": f"{n_rows} random rows of {name} in {c_secs:.1f}s (fp64 numpy, BLAS threads={threads})"}
 
     hbm_gbs, bf16_tf, src = load_peaks()
@@ -468,6 +508,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "lse_modes": lse_modes,
+        "warm_back_to_back": warm,
         "wall_s_timed_region": wall,
         "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "stages", "mma_n",
                                                                         "smem_bytes", "max_cta_cost",
@@ -492,6 +533,9 @@ def main():
     ap.add_argument("--no-lse-modes", action="store_true",
                     help="skip timing the forward-LSE and fused LSE+L1-norm launches")
     ap.add_argument("--lse-steps", type=int, default=50)
+    ap.add_argument("--no-warm", action="store_true", help="skip the back-to-back (warm L2) timing")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="configs 3 and 5 only: a shorter S1 = S2 of the same workload (small profiling case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -168,6 +168,31 @@ def test_run_from_host_pipelined_matches_run(lib, kind):
         pin["out"].fill_(float("nan"))
 
 
+def test_run_is_capturable_in_a_cuda_graph(lib):
+    """run() does host work only to encode the q tensor map and launches one
+    kernel (no allocation, no synchronisation), so it can be captured in a
+    CUDA graph; replays give the eager result bit for bit."""
+    w = W.make_workload(layout="BSND", dtype="bf16", B=1, S1=64, S2=1000, G=128, topk=512, mask_mode=3,
+                        seed=2860)
+    a, plan, t, _ = run_gpu(lib, w)
+    out = torch.full(plan.output_shape, float("nan"), dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture
+        plan.run(t["q"], t["k"], t["lse"], sparse_indices=t["idx"], topk_length=t["tl"], out=out, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        plan.run(t["q"], t["k"], t["lse"], sparse_indices=t["idx"], topk_length=t["tl"], out=out)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), a.view(np.uint32))
+    assert plan.status()[0] == lib.SMLA_OK
+
+
 def test_functional_api_matches_plan(lib):
     w = W.make_workload(layout="TND", dtype="bf16", seqlens_q=[33, 70], seqlens_k=[33, 90], G=16,
                         topk=64, mask_mode=3, seed=2800)

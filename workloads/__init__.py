@@ -454,6 +454,19 @@ def config_names():
     return dict(CONFIG_NAMES)
 
 
-def make_config(n: int, lse="estimate") -> Workload:
-    """Workload for configuration ``n`` (1..5)."""
-    return CONFIGS[n](lse=lse)
+def make_config(n: int, lse="estimate", seq_len=None) -> Workload:
+    """Workload for configuration ``n`` (1..5).  ``seq_len`` shortens the
+    square BSND configurations 3 and 5 (S1 = S2 = seq_len, same recipe and
+    seed; named with the length) -- a smaller case of the same workload, for
+    profiling captures that must stay small."""
+    if seq_len is None:
+        return CONFIGS[n](lse=lse)
+    if n not in (3, 5):
+        raise ValueError("seq_len applies to configurations 3 and 5")
+    S = int(seq_len)
+    if n == 3:
+        return make_workload(name=f"dsv32_sparse_causal_S{S}_G128_topk2048", layout="BSND", dtype="bf16",
+                             B=1, S1=S, S2=S, G=128, topk=2048, mask_mode=3, seed=3, lse=lse)
+    return make_workload(name=f"long_clustered_S{S}_G128_topk2048", layout="BSND", dtype="bf16",
+                         B=1, S1=S, S2=S, G=128, topk=2048, mask_mode=3, index_mode="clustered", seed=5,
+                         lse=lse)
