@@ -89,6 +89,31 @@ def test_s1_longer_than_s2_rows_without_keys(lib):
     assert np.all(got.reshape(40, -1)[:24] == 0.0)
 
 
+def test_no_key_rows_at_all(lib):
+    """S2 = 0: no key row exists, every slot is masked; the output is all
+    zero and the forward LSE is -inf (k may be NULL).  No key tile runs."""
+    w = W.make_workload(layout="BSND", dtype="bf16", B=2, S1=5, S2=0, G=16, topk=8, mask_mode=0,
+                        seed=2450, lse=None, with_topk_length=False)
+    w.sparse_indices = np.full(w.sparse_indices.shape, -1, np.int32)
+    W.set_lse_rows(w, np.zeros((w.n_tokens, w.G), np.float32))
+    plan = lib.Plan(**plan_kwargs(w))
+    t = to_device(w)
+    out = plan.run(t["q"], None, t["lse"], sparse_indices=t["idx"])
+    lse = plan.softmax_lse(t["q"], None, sparse_indices=t["idx"])
+    torch.cuda.synchronize()
+    assert np.all(out.cpu().numpy() == 0.0)
+    assert np.all(np.isneginf(lse.cpu().numpy()))
+    assert plan.status()[0] == lib.SMLA_OK  # no tile runs, so no index is read
+
+
+@pytest.mark.parametrize("topk,S2", [(8192, 9000), (1001, 1500)])
+def test_large_and_ragged_topk(lib, topk, S2):
+    """64 key tiles per token, and a topk that is no multiple of 4 or 16."""
+    w = W.make_workload(layout="BSND", dtype="bf16", B=1, S1=6, S2=S2, G=16, topk=topk, mask_mode=0,
+                        seed=2460 + topk, lse=None)
+    full_parity(lib, w)
+
+
 def test_bad_indices_are_masked_and_reported(lib):
     """No topk_length: every slot is a candidate; -1 is padding, other values
     outside [0, Sk) are masked and raise the bad-index warning."""
