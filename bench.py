@@ -281,8 +281,9 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     threads = host_threads()
-    r = cpu_oracle_run(args.config, args.warmup, args.steps, args.ref_step_seconds, threads,
-                       seq_len=args.seq_len)
+    # every step is a bounded sample; the whole run stays within --ref-total-seconds
+    step_s = max(0.02, min(args.ref_step_seconds, args.ref_total_seconds / max(1, args.steps)))
+    r = cpu_oracle_run(args.config, args.warmup, args.steps, step_s, threads, seq_len=args.seq_len)
     rows = sum(s[0] for s in r["steps"])
     pairs = sum(s[1] for s in r["steps"])
     secs = sum(s[2] for s in r["steps"])
@@ -298,7 +299,7 @@ def run_reference(args, world, rank):
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "cpu": cpu_model(),
                          "sample": f"{rows} random rows of {name} over {args.steps} steps "
-                                   f"(~{args.ref_step_seconds}s each)"},
+                                   f"(~{step_s:.2f}s each)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -529,7 +530,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0,
+                    help="reference arm: CPU seconds per step at most")
+    ap.add_argument("--ref-total-seconds", type=float, default=120.0,
+                    help="reference arm: CPU seconds over all timed steps at most")
     ap.add_argument("--no-lse-modes", action="store_true",
                     help="skip timing the forward-LSE and fused LSE+L1-norm launches")
     ap.add_argument("--lse-steps", type=int, default=50)

@@ -281,7 +281,10 @@ smla_status smla_l1norm_io_sizes(const smla_plan *plan, smla_io_sizes *sizes);
  * start after the work already queued on ``stream``, and ``stream`` waits
  * for the last copy, so to the caller the call is ordered on ``stream`` like
  * any other.  Otherwise (small problems) it is one copy per tensor, one
- * kernel and one copy back, all on ``stream``.
+ * kernel and one copy back, all on ``stream``.  The plan's streams and
+ * events are shared by its calls: issue run_from_host calls of one plan from
+ * one host thread at a time (calls queued on different streams are ordered
+ * through the plan's streams).
  */
 smla_status smla_l1norm_run_from_host(const smla_plan *plan,
                                       const void *h_q, const void *h_k, const float *h_lse,
