@@ -283,8 +283,9 @@ smla_status smla_l1norm_io_sizes(const smla_plan *plan, smla_io_sizes *sizes);
  * any other.  Otherwise (small problems) it is one copy per tensor, one
  * kernel and one copy back, all on ``stream``.  The plan's streams and
  * events are shared by its calls: issue run_from_host calls of one plan from
- * one host thread at a time (calls queued on different streams are ordered
- * through the plan's streams).
+ * one host thread at a time, and order calls that share device buffers on
+ * one stream (a later call's copies may otherwise overwrite inputs an
+ * earlier call's kernels still read).
  */
 smla_status smla_l1norm_run_from_host(const smla_plan *plan,
                                       const void *h_q, const void *h_k, const float *h_lse,
