@@ -67,8 +67,15 @@ def load_peaks():
 
 
 def kernel_sha():
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the kernel source with comments and blank lines removed, so
+    that edits to comments keep the profiled traffic valid."""
+    import re
+    with open(KERNEL_SRC, encoding="utf-8") as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    code = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def profiled_traffic(config_name):

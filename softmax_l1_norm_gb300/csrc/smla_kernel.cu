@@ -35,6 +35,12 @@
 // merges them with atomic adds; here one CTA owns a token's whole G x slots
 // block, so each output element is written once, in a fixed order.
 //
+// Modes (template parameter): the L1 norm from a given LSE (above); the
+// forward LSE the operator consumes, computed over the same kept slots (the
+// MMA issuers swap operands so that accumulator rows are q rows, and each
+// epilogue thread reduces its row over the keys with a running maximum);
+// and both in one launch, an LSE pass then an L1-norm pass per work item.
+//
 // Every mbarrier wait is bounded by a wall-clock limit; on expiry the kernel
 // records a timeout flag in the status word, all roles leave their loops,
 // outstanding copies and MMAs are waited for (again with a limit) and the
