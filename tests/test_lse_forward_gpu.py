@@ -165,7 +165,7 @@ def test_lse_large_logits_need_the_running_max(lib):
     assert lse.max() > 89.0
 
 
-@pytest.mark.parametrize("n", [3, 4])
+@pytest.mark.parametrize("n", [3, 4, 5])
 def test_lse_full_size_sampled(lib, n):
     """Full-size configuration in the launch configuration the benchmark
     times; the oracle checks a sample of rows."""
