@@ -292,15 +292,37 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMmaWarpA = 0;        // even head-dim chunks; sub-partition 0
 constexpr int kMmaWarpB = 2;        // odd head-dim chunks; sub-partition 2
 constexpr int kQWarp = 8;           // sleeps in barrier waits most of the time
-constexpr int kProducerWarps = 4;   // warps 1, 3, 9, 11 (sub-partitions 1 and 3)
+constexpr int kProducerWarps = 4;   // warps of a producer group (one stage at a time)
 constexpr int kKeysPerLane = kTileKeys / (kProducerWarps * 4);   // 8
+// Producer groups.  A lane's cp.async.mbarrier.arrive.noinc completes once
+// all of the lane's earlier copies have landed, which holds a producer
+// group to about one stage in flight: ~30 B/clk per SM whatever the number
+// of warps sharing the stage (measured).  The L1-norm mode therefore runs
+// two groups of 4 warps on alternate stages (even / odd head-dim chunks),
+// in 16 warps; the LSE modes keep one group in 12 warps, as their epilogue
+// needs more registers than 16 warps leave.
+template <int kMode>
+__host__ __device__ constexpr int producer_groups() {
+  return kMode == kModeL1 ? 2 : 1;
+}
+template <int kMode>
+__host__ __device__ constexpr int kernel_threads() {
+  return kMode == kModeL1 ? 512 : kThreads;
+}
 constexpr int kEpiWarp0 = 4;        // warps 4-7: one warpgroup
+// Producer warp number: group 0 = warps 1, 3, 9, 11 (sub-partitions 1 and
+// 3); group 1 = warps 13, 15, 10, 14.
+template <int kMode>
 __device__ __forceinline__ int producer_index(int warp) {
   switch (warp) {
     case 1: return 0;
     case 3: return 1;
     case 9: return 2;
     case 11: return 3;
+    case 13: return producer_groups<kMode>() > 1 ? 4 : -1;
+    case 15: return producer_groups<kMode>() > 1 ? 5 : -1;
+    case 10: return producer_groups<kMode>() > 1 ? 6 : -1;
+    case 14: return producer_groups<kMode>() > 1 ? 7 : -1;
     default: return -1;
   }
 }
@@ -479,7 +501,7 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
 }  // namespace
 
 template <bool kSparse, int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
     smla_fused_kernel(const __grid_constant__ KernelParams p,
                       const __grid_constant__ CUtensorMap tmap_q) {
   extern __shared__ uint8_t smem_raw[];
@@ -551,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int it0 = p.cta_begin[blockIdx.x];
   const int it1 = p.cta_begin[blockIdx.x + 1];
 
-  const int pw = producer_index(warp);
+  const int pw = producer_index<kMode>(warp);
   if (pw >= 0) {
     // ============================================================ key producers
     // Producer warp pw, lane l copies 16-byte segment (l & 7) of key rows
@@ -563,10 +585,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // generic-to-async proxy fence the tensor cores need is executed by the
     // MMA thread after it acquires the full barrier: in a producer it would
     // also wait for the copies still in flight.
+    const int grp = pw / kProducerWarps;  // this group fills the chunks c with c % groups == grp
     const int seg = lane & 7;
-    const int krow0 = pw * (kTileKeys / kProducerWarps) + (lane >> 3);
+    const int krow0 = (pw % kProducerWarps) * (kTileKeys / kProducerWarps) + (lane >> 3);
     const uint32_t S = static_cast<uint32_t>(p.stages);
-    uint32_t kst = 0, kph = 0;   // slot being filled, its phase
+    constexpr uint32_t kStep = producer_groups<kMode>();  // stages between this group's stages
+    uint32_t kst = grp, kph = 0;  // slot of this group's next stage, its phase (S > kStep)
     bool ok = true;
     TileCursor cur{it0 - 1, 0, 0, 0, 0, WorkItem{}};
     bool have = cursor_next<kSparse, kMode>(p, cur, it1);
@@ -598,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileCursor nxt = cur;
       const bool have_next = cursor_next<kSparse, kMode>(p, nxt, it1);
       if (have_next) fetch_indices(nxt);  // in flight while this tile streams
-      for (int c = 0; c < kNumChunks; ++c) {
+      for (int c = grp; c < kNumChunks; c += kStep) {
         ok = __all_sync(0xffffffffu, wait_bounded(bar_k_empty + 8 * kst, kph ^ 1u, ctl));
         if (!ok) break;
         const uint32_t dst = sK + kst * kKStageBytes;
@@ -608,8 +632,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           cp_async_16(dst + r * 128 + ((seg ^ (r & 7)) << 4), src[i] + c * (kChunkElems * 2));
         }
         cp_async_arrive_noinc(bar_k_full + 8 * kst);
-        kst = (kst + 1 == S) ? 0u : kst + 1;
-        kph ^= (kst == 0) ? 1u : 0u;
+        kst += kStep;
+        if (kst >= S) {
+          kst -= S;
+          kph ^= 1u;
+        }
       }
       cur = nxt;
       have = have_next;
@@ -936,10 +963,11 @@ cudaError_t configure_fused(int smem_bytes) {
 
 cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int mode, int grid,
                          int smem_bytes, cudaStream_t stream) {
-  const dim3 g(grid), b(kThreads);
+  const dim3 g(grid);
+  const dim3 b1(kernel_threads<kModeL1>()), b(kThreads);
   switch (mode * 2 + (sparse ? 1 : 0)) {
-    case kModeL1 * 2 + 1: smla_fused_kernel<true, kModeL1><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
-    case kModeL1 * 2: smla_fused_kernel<false, kModeL1><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeL1 * 2 + 1: smla_fused_kernel<true, kModeL1><<<g, b1, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeL1 * 2: smla_fused_kernel<false, kModeL1><<<g, b1, smem_bytes, stream>>>(p, tmap_q); break;
     case kModeLse * 2 + 1: smla_fused_kernel<true, kModeLse><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
     case kModeLse * 2: smla_fused_kernel<false, kModeLse><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
     case kModeFused * 2 + 1: smla_fused_kernel<true, kModeFused><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
