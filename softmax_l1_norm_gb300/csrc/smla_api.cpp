@@ -222,9 +222,11 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
   return s;
 }
 
+// Deepest key ring that fits, with an even number of slots (the kernel's
+// barrier phases rely on it when several producer groups fill the ring).
 int stages_for(int n_mma, int smem_limit) {
   int st = smla::kMaxStages;
-  while (st > 2 && smla::smem_bytes_for(n_mma, st) > smem_limit) --st;
+  while (st > smla::kMinStages && smla::smem_bytes_for(n_mma, st) > smem_limit) st -= 2;
   return st;
 }
 

@@ -26,7 +26,11 @@ constexpr int kAccCols = 256;
 constexpr int kHalfCols = 128;
 constexpr int kMaxN = 128;  // largest MMA N (R*G padded to 16)
 constexpr int kMaxStages = 12;
-constexpr int kThreads = 384;  // 12 warps: 2 MMA issuers, 4 key producers, one epilogue warpgroup, q loader, 1 spare
+// The key ring holds an even number of stages, at least as many as there are
+// producer groups (a group's next stage is that many chunks after its
+// previous one).
+constexpr int kMinStages = 4;
+constexpr int kThreads = 384;  // LSE modes: 2 MMA issuers, 4 key producers, one epilogue warpgroup, q loader, 1 spare
 
 // Status word bits.
 constexpr int kFlagBadIndex = 1;

@@ -7,14 +7,18 @@
 //     out[i] = 0                                                   otherwise
 // with j_i = sparse_indices[i] (stage 1 gather) or j_i = i (dense form).
 //
-// How (one persistent CTA per SM, 384 threads, warp-specialised):
-//   warps 1, 3, 9, 11  key producers.  Each 128-key tile is moved in 8 stages of
-//               64 head-dim columns (128 keys x 128 bytes = 16 KB).  Every
-//               thread copies 16-byte pieces with cp.async straight into the
-//               128-byte-swizzle position the MMA descriptor expects (a warp
-//               instruction covers 4 whole 128-byte key rows), so any key
-//               order costs the same as a contiguous tile.  The key indices
-//               of the next tile are fetched while the current tile streams.
+// How (one persistent CTA per SM, warp-specialised: 512 threads for the L1
+// norm, 384 for the LSE modes):
+//   key producers (warps 1, 3, 9, 11, and 13, 15, 10, 14 for the L1 norm).
+//               Each 128-key tile is moved in 8 stages of 64 head-dim columns
+//               (128 keys x 128 bytes = 16 KB), each stage by one group of
+//               four warps (two groups take turns in the L1-norm mode).
+//               Every thread copies 16-byte
+//               pieces with cp.async straight into the 128-byte-swizzle
+//               position the MMA descriptor expects (a warp instruction
+//               covers 4 whole 128-byte key rows), so any key order costs the
+//               same as a contiguous tile.  The key indices of the next tile
+//               are fetched while the current tile streams.
 //   warps 0, 2  MMA issuers.  tcgen05.mma kind::f16, M = 128 keys (A = key
 //               stage), N = G heads padded to 16 (B = q chunk), K = 512 in
 //               32 steps of 16, fp32 accumulation in TMEM.  One thread cannot
@@ -292,40 +296,57 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMmaWarpA = 0;        // even head-dim chunks; sub-partition 0
 constexpr int kMmaWarpB = 2;        // odd head-dim chunks; sub-partition 2
 constexpr int kQWarp = 8;           // sleeps in barrier waits most of the time
-constexpr int kProducerWarps = 4;   // warps of a producer group (one stage at a time)
-constexpr int kKeysPerLane = kTileKeys / (kProducerWarps * 4);   // 8
-// Producer groups.  A lane's cp.async.mbarrier.arrive.noinc completes once
-// all of the lane's earlier copies have landed, which holds a producer
-// group to about one stage in flight: ~30 B/clk per SM whatever the number
-// of warps sharing the stage (measured).  The L1-norm mode therefore runs
-// two groups of 4 warps on alternate stages (even / odd head-dim chunks),
-// in 16 warps; the LSE modes keep one group in 12 warps, as their epilogue
-// needs more registers than 16 warps leave.
+// Producer groups.  A lane's cp.async.mbarrier.arrive.noinc holds the warp
+// until every copy the lane issued before it has landed, so a warp keeps
+// one batch of copies in flight and pays about one loaded L2 round trip per
+// arrive (measured on all 152 SMs: 8 copies of 512 B per warp between
+// arrives give ~7.5 B/clk per warp, 16 give ~13, whatever the ring depth).
+// A group of warps fills one stage; several groups fill alternate stages
+// (group g fills the head-dim chunks c with c % groups == g).  The L1-norm
+// mode runs 2 groups of 4 warps in 16 warps; the LSE modes one group of 4
+// in 12 warps, as their epilogue needs more registers than 16 warps leave.
+// A group's next stage follows its previous one by `groups` chunks; with an
+// even number of ring slots, at least `groups` of them, no full or empty
+// barrier is ever two phases behind a thread that waits on it.
 template <int kMode>
 __host__ __device__ constexpr int producer_groups() {
   return kMode == kModeL1 ? 2 : 1;
 }
 template <int kMode>
+__host__ __device__ constexpr int group_warps() {
+  return 4;
+}
+template <int kMode>
+__host__ __device__ constexpr int keys_per_lane() {  // 4 key rows per warp instruction
+  return kTileKeys / (group_warps<kMode>() * 4);
+}
+static_assert(kTileKeys % 16 == 0 && kNumChunks % 4 == 0, "groups own the same chunks of every tile");
+static_assert(kMinStages >= 4 && kMinStages % 2 == 0, "ring depth rule");
+template <int kMode>
 __host__ __device__ constexpr int kernel_threads() {
   return kMode == kModeL1 ? 512 : kThreads;
 }
 constexpr int kEpiWarp0 = 4;        // warps 4-7: one warpgroup
-// Producer warp number: group 0 = warps 1, 3, 9, 11 (sub-partitions 1 and
-// 3); group 1 = warps 13, 15, 10, 14.
+// Producer warp number: warps 1, 3, 9, 11 (sub-partitions 1 and 3), then,
+// for a second group, 13, 15, 10, 14.
 template <int kMode>
 __device__ __forceinline__ int producer_index(int warp) {
+  constexpr int n = producer_groups<kMode>() * group_warps<kMode>();
+  int i;
   switch (warp) {
-    case 1: return 0;
-    case 3: return 1;
-    case 9: return 2;
-    case 11: return 3;
-    case 13: return producer_groups<kMode>() > 1 ? 4 : -1;
-    case 15: return producer_groups<kMode>() > 1 ? 5 : -1;
-    case 10: return producer_groups<kMode>() > 1 ? 6 : -1;
-    case 14: return producer_groups<kMode>() > 1 ? 7 : -1;
-    default: return -1;
+    case 1: i = 0; break;
+    case 3: i = 1; break;
+    case 9: i = 2; break;
+    case 11: i = 3; break;
+    case 13: i = 4; break;
+    case 15: i = 5; break;
+    case 10: i = 6; break;
+    case 14: i = 7; break;
+    default: i = 8;
   }
+  return i < n ? i : -1;
 }
+static_assert(producer_groups<kModeL1>() * group_warps<kModeL1>() <= 8, "8 producer warps at most");
 
 // Lengths of an item's sequence that take part in the computation: the
 // full lengths, cut to seqused_q[b] / seqused_k[b] when those are given
@@ -423,8 +444,18 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
   const uint32_t k_lo0 = static_cast<uint32_t>(a0), q_lo0 = static_cast<uint32_t>(b0);
   const uint32_t b_step = static_cast<uint32_t>(m.q_chunk_bytes) >> 4;
   const uint32_t S = static_cast<uint32_t>(p.stages);
-  uint32_t kst = 0, kph = 0, qit = 0, acc = 0;
+  // Ring slot and phase of this issuer's next stage: stage n (8 per tile,
+  // tile-major) uses slot n % S, and this issuer takes every other stage.
+  uint32_t kst = H, kph = 0, qit = 0, acc = 0;
   bool ok = true;
+  // The barrier test for this issuer's next stage is issued before the
+  // current stage's MMAs (and across tile boundaries) so that its latency
+  // overlaps them; only a stage that is not ready yet costs a blocking wait.
+  // A stage acquired by that test before a proxy fence is covered by the
+  // fence and needs none of its own (with copies in flight a fence waits for
+  // all of them).  The accumulator buffer of the next tile is tested the
+  // same way.
+  bool ready = false, covered = false, acc_ready = false;
   WorkItem w_next = m.it0 < m.it1 ? p.items[m.it0] : WorkItem{};
   for (int it = m.it0; it < m.it1 && ok; ++it) {
     const WorkItem w = w_next;
@@ -433,35 +464,28 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
     const int nt = item_tiles<kSparse>(p, w, tl);
     if (nt == 0) continue;
     const uint32_t qpar = qit & 1u;
-    for (int t = 0; t < nt * passes<kMode>() && ok; ++t, ++acc) {
+    const int ntot = nt * passes<kMode>();
+    for (int t = 0; t < ntot && ok; ++t, ++acc) {
       const uint32_t buf = acc & (kAccBufs - 1);
-      ok = wait_bounded(m.bar_acc_empty + 8 * buf, ((acc / kAccBufs) & 1u) ^ 1u, ctl);
-      if (!ok) break;
+      if (!acc_ready) {
+        ok = wait_bounded(m.bar_acc_empty + 8 * buf, ((acc / kAccBufs) & 1u) ^ 1u, ctl);
+        if (!ok) break;
+      }
       tc_fence_after();
       const uint32_t d_tmem = m.tmem_base + buf * kAccCols + H * kHalfCols;
-      const bool last = (t == nt * passes<kMode>() - 1);
+      const bool last = (t == ntot - 1);
       const bool lse_pass = kMode != kModeL1 && t < nt;
       const uint32_t idesc = static_cast<uint32_t>(lse_pass ? p.idesc_lse : p.idesc);
-      // ring slot and phase of each of the tile's 8 stages
-      uint32_t sl[kNumChunks], ph[kNumChunks];
-#pragma unroll
-      for (int c = 0; c < kNumChunks; ++c) {
-        sl[c] = kst;
-        ph[c] = kph;
-        kst = (kst + 1 == S) ? 0u : kst + 1;
-        kph ^= (kst == 0) ? 1u : 0u;
-      }
-      // The barrier test for the next stage is issued before the current
-      // stage's MMAs so that its latency overlaps them; only a stage that is
-      // not ready yet costs a blocking wait.  A stage already acquired by
-      // that test before a proxy fence is covered by the fence and needs
-      // none of its own (with copies in flight a fence waits for all of them).
-      bool ready = mbar_test_wait(m.bar_k_full + 8 * sl[H], ph[H]);
-      bool covered = false;
 #pragma unroll
       for (int c = H; c < kNumChunks; c += 2) {
+        const uint32_t sl = kst, ph = kph;
+        kst += 2;
+        if (kst >= S) {
+          kst -= S;
+          kph ^= 1u;
+        }
         if (!ready) {
-          ok = wait_bounded(m.bar_k_full + 8 * sl[c], ph[c], ctl);
+          ok = wait_bounded(m.bar_k_full + 8 * sl, ph, ctl);
           if (!ok) break;
         }
         // q chunk c of a new token was freed about 8 stages ago
@@ -469,13 +493,15 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
           ok = wait_bounded(m.bar_q_full + 8 * c, qpar, ctl);
           if (!ok) break;
         }
-        const bool ready_next = (c + 2 < kNumChunks) ? mbar_test_wait(m.bar_k_full + 8 * sl[c + 2], ph[c + 2]) : false;
+        const bool ready_next = mbar_test_wait(m.bar_k_full + 8 * kst, kph);
+        if (c + 2 >= kNumChunks)
+          acc_ready = mbar_test_wait(m.bar_acc_empty + 8 * (buf ^ 1u), (((acc + 1) / kAccBufs) & 1u) ^ 1u);
         // the producers' cp.async writes (generic proxy), acquired through
         // the barrier, become visible to the tensor cores (async proxy)
         if (!covered) fence_proxy_async();
         covered = ready_next;
         tc_fence_after();
-        const uint32_t k_lo = k_lo0 + sl[c] * (kKStageBytes >> 4);
+        const uint32_t k_lo = k_lo0 + sl * (kKStageBytes >> 4);
         const uint32_t q_lo = q_lo0 + c * b_step;
         const uint32_t a_lo = lse_pass ? q_lo : k_lo;
         const uint32_t b_lo = lse_pass ? k_lo : q_lo;
@@ -487,7 +513,7 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
         umma_f16_lohi<true>(d_tmem, a_lo + 2, a_hi, b_lo + 2, b_hi, idesc);
         umma_f16_lohi<true>(d_tmem, a_lo + 4, a_hi, b_lo + 4, b_hi, idesc);
         umma_f16_lohi<true>(d_tmem, a_lo + 6, a_hi, b_lo + 6, b_hi, idesc);
-        umma_commit(m.bar_k_empty + 8 * sl[c]);
+        umma_commit(m.bar_k_empty + 8 * sl);
         if (last) umma_commit(m.bar_q_empty + 8 * c);
         ready = ready_next;
       }
@@ -538,7 +564,7 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
       mbar_init(bar_q_empty + 8 * c, 1);
     }
     for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(bar_k_full + 8 * s, kProducerWarps * 32);
+      mbar_init(bar_k_full + 8 * s, group_warps<kMode>() * 32);
       mbar_init(bar_k_empty + 8 * s, 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
@@ -576,21 +602,24 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
   const int pw = producer_index<kMode>(warp);
   if (pw >= 0) {
     // ============================================================ key producers
-    // Producer warp pw, lane l copies 16-byte segment (l & 7) of key rows
-    // pw*32 + (l >> 3) + 4*i, i = 0..7, of every stage (4 whole 128-byte
-    // rows per warp instruction).  Stage n uses ring slot n % stages.  Each
-    // lane's copies arrive on the slot's full barrier by themselves when
-    // they land (cp.async.mbarrier.arrive.noinc), so a producer only waits
-    // for free slots and every slot of the ring can be in flight.  The
-    // generic-to-async proxy fence the tensor cores need is executed by the
-    // MMA thread after it acquires the full barrier: in a producer it would
-    // also wait for the copies still in flight.
-    const int grp = pw / kProducerWarps;  // this group fills the chunks c with c % groups == grp
+    // Producer warp pw of group grp, lane l copies 16-byte segment (l & 7)
+    // of key rows r0 + (l >> 3) + 4*i, i < keys_per_lane, of each of its
+    // group's stages (4 whole 128-byte rows per warp instruction), r0 =
+    // (pw % group_warps) * 128 / group_warps.  Stage n uses ring slot
+    // n % stages.  Each lane's copies arrive on the slot's full barrier by
+    // themselves when they land (cp.async.mbarrier.arrive.noinc), so a
+    // producer only waits for free slots.  The generic-to-async proxy fence
+    // the tensor cores need is executed by the MMA thread after it acquires
+    // the full barrier: in a producer it would also wait for the copies
+    // still in flight.
+    constexpr int kGW = group_warps<kMode>();
+    constexpr int kKeysPerLane = keys_per_lane<kMode>();
+    const int grp = pw / kGW;
     const int seg = lane & 7;
-    const int krow0 = (pw % kProducerWarps) * (kTileKeys / kProducerWarps) + (lane >> 3);
+    const int krow0 = (pw % kGW) * (kTileKeys / kGW) + (lane >> 3);
     const uint32_t S = static_cast<uint32_t>(p.stages);
-    constexpr uint32_t kStep = producer_groups<kMode>();  // stages between this group's stages
-    uint32_t kst = grp, kph = 0;  // slot of this group's next stage, its phase (S > kStep)
+    constexpr uint32_t kStep = producer_groups<kMode>();  // chunks between this group's stages
+    uint32_t kst = grp, kph = 0;  // slot of this group's next stage and its phase (S >= kStep)
     bool ok = true;
     TileCursor cur{it0 - 1, 0, 0, 0, 0, WorkItem{}};
     bool have = cursor_next<kSparse, kMode>(p, cur, it1);
@@ -607,16 +636,17 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
       }
     };
     if (have) fetch_indices(cur);
+    const uint8_t* kseg = p.k + seg * 16;
     while (have && ok) {
-      // source rows of this tile (invalid slots read key 0 of the sequence)
-      const uint8_t* src[kKeysPerLane];
+      // source key rows of this tile (invalid slots read key 0 of the sequence)
+      int64_t row[kKeysPerLane];
       bool bad = false;
 #pragma unroll
       for (int i = 0; i < kKeysPerLane; ++i) {
         const int j = jn[i];
         const bool in = (j >= 0) && (j < cur.w.Sk);
         if (kSparse) bad |= (krow0 + 4 * i + cur.ktile() * kTileKeys < cur.tl) && !in && (j != -1);
-        src[i] = p.k + (static_cast<int64_t>(cur.w.k_base) + (in ? j : 0)) * (kHeadDim * 2) + seg * 16;
+        row[i] = static_cast<int64_t>(cur.w.k_base) + (in ? j : 0);
       }
       if (kSparse && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kFlagBadIndex);
       TileCursor nxt = cur;
@@ -626,10 +656,11 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
         ok = __all_sync(0xffffffffu, wait_bounded(bar_k_empty + 8 * kst, kph ^ 1u, ctl));
         if (!ok) break;
         const uint32_t dst = sK + kst * kKStageBytes;
+        const uint8_t* kc = kseg + c * (kChunkElems * 2);
 #pragma unroll
         for (int i = 0; i < kKeysPerLane; ++i) {
           const int r = krow0 + 4 * i;
-          cp_async_16(dst + r * 128 + ((seg ^ (r & 7)) << 4), src[i] + c * (kChunkElems * 2));
+          cp_async_16(dst + r * 128 + ((seg ^ (r & 7)) << 4), kc + row[i] * (kHeadDim * 2));
         }
         cp_async_arrive_noinc(bar_k_full + 8 * kst);
         kst += kStep;
