@@ -269,6 +269,27 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Two fp32 lanes in one 64-bit register: Blackwell's packed f32x2
+// add and fma round each lane exactly as the scalar instructions do.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // Named barriers for one epilogue warpgroup (ids 1 and 2; 0 is __syncthreads).
 __device__ __forceinline__ void wg_sync(int id) {
   asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
@@ -724,14 +745,13 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
     // ============================================================ epilogue
     const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
     const int et = quarter * 32 + lane;      // TMEM lane: key slot (L1 pass) or q row (LSE pass)
-    float* L = ltab;
+    float* NL = ltab;  // -lse * log2(e) per accumulator column (L1-norm pass)
     constexpr int bar_id = 1;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t acc = 0;
     bool ok = true;
     const float c2 = p.c_log2;
     const float neg_inf = __int_as_float(0xff800000);
-    const float pos_inf = __int_as_float(0x7f800000);
     for (int it = it0; it < it1 && ok; ++it) {
       const WorkItem w = p.items[it];
       int tl;
@@ -832,20 +852,20 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
         if (kMode == kModeFused && nt > 0) {
           // the L1 pass reads the LSE per accumulator column
           wg_sync(bar_id);
-          if (et < p.n_mma) L[et] = et < w.nrows * p.G ? lse2 : pos_inf;
+          if (et < p.n_mma) NL[et] = et < w.nrows * p.G ? -lse2 : neg_inf;
           wg_sync(bar_id);
         }
       }
       if (kMode == kModeLse) continue;
       // ---------------------------------------------------- L1-norm pass
       if (kMode == kModeL1 && nt > 0) {
-        // lse * log2(e) per accumulator column; +inf beyond the real heads
+        // -lse * log2(e) per accumulator column; -inf beyond the real heads
         // so that padded columns contribute exp2(-inf) = 0.
         wg_sync(bar_id);
         if (et < p.n_mma) {
-          float v = pos_inf;
-          if (et < w.nrows * p.G) v = __ldg(p.lse + static_cast<int64_t>(w.q_tok) * p.G + et) * kLog2e;
-          L[et] = v;
+          float v = neg_inf;
+          if (et < w.nrows * p.G) v = -(__ldg(p.lse + static_cast<int64_t>(w.q_tok) * p.G + et) * kLog2e);
+          NL[et] = v;
         }
         wg_sync(bar_id);
       }
@@ -870,13 +890,21 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
         const uint32_t taddr = tmem_base + lane_addr + buf * kAccCols;
         if (kSparse) {
           // sum over the heads of exp2(s * scale * log2(e) - lse * log2(e)),
-          // 16 columns at a time, the next 16 loading meanwhile
-          float s0 = 0.f, s1 = 0.f;
+          // 16 columns at a time, the next 16 loading meanwhile; columns in
+          // pairs (packed f32x2 add and fma), even and odd columns summed
+          // in separate lanes
+          uint64_t s01 = 0;  // (0.f, 0.f)
+          const uint64_t c2c2 = pack_f32x2(c2, c2);
           auto l1_16 = [&](const uint32_t (&fa)[16], const uint32_t (&ga)[16], int c0) {
+            const float2* nl2 = reinterpret_cast<const float2*>(NL + c0);
 #pragma unroll
             for (int k = 0; k < 16; k += 2) {
-              s0 += fast_exp2(fmaf(__uint_as_float(fa[k]) + __uint_as_float(ga[k]), c2, -L[c0 + k]));
-              s1 += fast_exp2(fmaf(__uint_as_float(fa[k + 1]) + __uint_as_float(ga[k + 1]), c2, -L[c0 + k + 1]));
+              const float2 nl = nl2[k / 2];
+              const uint64_t x = add_f32x2(pack_f32x2(__uint_as_float(fa[k]), __uint_as_float(fa[k + 1])),
+                                           pack_f32x2(__uint_as_float(ga[k]), __uint_as_float(ga[k + 1])));
+              float y0, y1;
+              unpack_f32x2(fma_f32x2(x, c2c2, pack_f32x2(nl.x, nl.y)), y0, y1);
+              s01 = add_f32x2(s01, pack_f32x2(fast_exp2(y0), fast_exp2(y1)));
             }
           };
           const int n = p.n_mma;  // a multiple of 16
@@ -902,6 +930,8 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
           }
           tc_fence_before();
           mbar_arrive(bar_acc_empty + 8 * buf);
+          float s0, s1;
+          unpack_f32x2(s01, s0, s1);
           if (slot < p.topk)
             p.out[static_cast<int64_t>(w.q_tok) * p.topk + slot] = valid ? (s0 + s1) * p.inv_g : 0.f;
         } else {
@@ -915,7 +945,7 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
             tmem_ld16(taddr + kHalfCols + c0, g);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              s += fast_exp2(fmaf(f[k] + g[k], c2, -L[c0 + k]));
+              s += fast_exp2(fmaf(f[k] + g[k], c2, NL[c0 + k]));
               if (++g_in == p.G) {
                 if (r < w.nrows && j < p.width) {
                   const bool v = (j < e.Sk) && (w.r0 + r < e.Sq) &&

@@ -86,7 +86,7 @@ def lse_parity(lib, w, su_q=None, su_k=None, expect=None, rows=None):
     return lse_rows, got
 
 
-@pytest.mark.parametrize("G", [1, 8, 64, 128])
+@pytest.mark.parametrize("G", [1, 8, 64, 100, 128])
 def test_lse_sparse_heads_multi_tile_ragged(lib, G):
     w = W.make_workload(layout="BSND", dtype="bf16", B=2, S1=24, S2=700, G=G, topk=300, mask_mode=3,
                         seed=5000 + G, lse=None)
