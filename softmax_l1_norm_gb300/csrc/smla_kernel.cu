@@ -284,6 +284,11 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
@@ -751,6 +756,7 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
     uint32_t acc = 0;
     bool ok = true;
     const float c2 = p.c_log2;
+    const uint64_t c2c2 = pack_f32x2(c2, c2);
     const float neg_inf = __int_as_float(0xff800000);
     for (int it = it0; it < it1 && ok; ++it) {
       const WorkItem w = p.items[it];
@@ -802,12 +808,21 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
           // the sum is split over four chains.  The loop is kept rolled: the
           // warps of all roles share the instruction cache.
           const int lim = limit - t * kTileKeys;  // dense form: columns c < lim are kept
+          // Column pairs go through packed f32x2 add / mul (each lane rounded
+          // as the scalar instruction rounds it).
           auto lse16 = [&](const uint32_t (&fa)[16], const uint32_t (&ga)[16], int c0, uint32_t bits16) {
             float x[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const bool keep = kSparse ? ((bits16 >> k) & 1u) != 0 : (c0 + k < lim);
-              x[k] = keep ? (__uint_as_float(fa[k]) + __uint_as_float(ga[k])) * c2 : neg_inf;
+            for (int k = 0; k < 16; k += 2) {
+              float v0, v1;
+              unpack_f32x2(mul_f32x2(add_f32x2(pack_f32x2(__uint_as_float(fa[k]), __uint_as_float(fa[k + 1])),
+                                               pack_f32x2(__uint_as_float(ga[k]), __uint_as_float(ga[k + 1]))),
+                                     c2c2),
+                           v0, v1);
+              const bool keep0 = kSparse ? ((bits16 >> k) & 1u) != 0 : (c0 + k < lim);
+              const bool keep1 = kSparse ? ((bits16 >> (k + 1)) & 1u) != 0 : (c0 + k + 1 < lim);
+              x[k] = keep0 ? v0 : neg_inf;
+              x[k + 1] = keep1 ? v1 : neg_inf;
             }
             float t8[8];
 #pragma unroll
@@ -819,10 +834,21 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
               m = cm;
             }
             if (m != neg_inf) {
-              float s4[4] = {0.f, 0.f, 0.f, 0.f};
+              // four chains: columns k % 4 == 0, 1 (lanes of s01) and 2, 3 (s23)
+              uint64_t s01 = 0, s23 = 0;
+              const uint64_t nm = pack_f32x2(-m, -m);
 #pragma unroll
-              for (int k = 0; k < 16; ++k) s4[k & 3] += fast_exp2(x[k] - m);
-              sum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+              for (int k = 0; k < 16; k += 4) {
+                float d0, d1, d2, d3;
+                unpack_f32x2(add_f32x2(pack_f32x2(x[k], x[k + 1]), nm), d0, d1);
+                unpack_f32x2(add_f32x2(pack_f32x2(x[k + 2], x[k + 3]), nm), d2, d3);
+                s01 = add_f32x2(s01, pack_f32x2(fast_exp2(d0), fast_exp2(d1)));
+                s23 = add_f32x2(s23, pack_f32x2(fast_exp2(d2), fast_exp2(d3)));
+              }
+              float s0, s1, s2, s3;
+              unpack_f32x2(s01, s0, s1);
+              unpack_f32x2(s23, s2, s3);
+              sum += (s0 + s1) + (s2 + s3);
             }
           };
           uint32_t fa[16], ga[16], fb[16], gb[16];
@@ -890,21 +916,31 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
         const uint32_t taddr = tmem_base + lane_addr + buf * kAccCols;
         if (kSparse) {
           // sum over the heads of exp2(s * scale * log2(e) - lse * log2(e)),
-          // 16 columns at a time, the next 16 loading meanwhile; columns in
-          // pairs (packed f32x2 add and fma), even and odd columns summed
-          // in separate lanes
+          // 16 columns at a time, the next 16 loading meanwhile; even and
+          // odd columns are summed separately.  The L1-norm launch works on
+          // column pairs with packed f32x2 add and fma (each lane rounded as
+          // the scalar instructions round it); the fused launch keeps the
+          // scalar form, which measured faster there.
           uint64_t s01 = 0;  // (0.f, 0.f)
-          const uint64_t c2c2 = pack_f32x2(c2, c2);
+          float s0 = 0.f, s1 = 0.f;
           auto l1_16 = [&](const uint32_t (&fa)[16], const uint32_t (&ga)[16], int c0) {
-            const float2* nl2 = reinterpret_cast<const float2*>(NL + c0);
+            if constexpr (kMode == kModeL1) {
+              const float2* nl2 = reinterpret_cast<const float2*>(NL + c0);
 #pragma unroll
-            for (int k = 0; k < 16; k += 2) {
-              const float2 nl = nl2[k / 2];
-              const uint64_t x = add_f32x2(pack_f32x2(__uint_as_float(fa[k]), __uint_as_float(fa[k + 1])),
-                                           pack_f32x2(__uint_as_float(ga[k]), __uint_as_float(ga[k + 1])));
-              float y0, y1;
-              unpack_f32x2(fma_f32x2(x, c2c2, pack_f32x2(nl.x, nl.y)), y0, y1);
-              s01 = add_f32x2(s01, pack_f32x2(fast_exp2(y0), fast_exp2(y1)));
+              for (int k = 0; k < 16; k += 2) {
+                const float2 nl = nl2[k / 2];
+                const uint64_t x = add_f32x2(pack_f32x2(__uint_as_float(fa[k]), __uint_as_float(fa[k + 1])),
+                                             pack_f32x2(__uint_as_float(ga[k]), __uint_as_float(ga[k + 1])));
+                float y0, y1;
+                unpack_f32x2(fma_f32x2(x, c2c2, pack_f32x2(nl.x, nl.y)), y0, y1);
+                s01 = add_f32x2(s01, pack_f32x2(fast_exp2(y0), fast_exp2(y1)));
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < 16; k += 2) {
+                s0 += fast_exp2(fmaf(__uint_as_float(fa[k]) + __uint_as_float(ga[k]), c2, NL[c0 + k]));
+                s1 += fast_exp2(fmaf(__uint_as_float(fa[k + 1]) + __uint_as_float(ga[k + 1]), c2, NL[c0 + k + 1]));
+              }
             }
           };
           const int n = p.n_mma;  // a multiple of 16
@@ -930,8 +966,7 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
           }
           tc_fence_before();
           mbar_arrive(bar_acc_empty + 8 * buf);
-          float s0, s1;
-          unpack_f32x2(s01, s0, s1);
+          if constexpr (kMode == kModeL1) unpack_f32x2(s01, s0, s1);
           if (slot < p.topk)
             p.out[static_cast<int64_t>(w.q_tok) * p.topk + slot] = valid ? (s0 + s1) * p.inv_g : 0.f;
         } else {
