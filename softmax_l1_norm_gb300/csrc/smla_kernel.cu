@@ -216,27 +216,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                    bar)
                : "memory");
 }
-// 16 consecutive fp32 accumulator columns of this thread's TMEM lane; the
-// wait is fused so the registers are only read once the load completed.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&f)[16]) {
-  uint32_t v[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
-      " [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
-                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15])
-               :
-               : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
-}
-
 // Split form for software pipelining: issue the loads of the next 16
 // columns of both accumulator halves, work on the current ones, then wait.
 // The wait names the in-flight registers so that no use of them moves
@@ -970,17 +949,15 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
           if (slot < p.topk)
             p.out[static_cast<int64_t>(w.q_tok) * p.topk + slot] = valid ? (s0 + s1) * p.inv_g : 0.f;
         } else {
-          // Dense form: columns r*G + g belong to token q_tok + r.
+          // Dense form: columns r*G + g belong to token q_tok + r; 16
+          // columns at a time, the next 16 loading meanwhile.
           const int j = slot;
           float s = 0.f;
           int g_in = 0, r = 0;
-          for (int c0 = 0; c0 < p.n_mma; c0 += 16) {
-            float f[16], g[16];
-            tmem_ld16(taddr + c0, f);
-            tmem_ld16(taddr + kHalfCols + c0, g);
+          auto dense16 = [&](const uint32_t (&fa)[16], const uint32_t (&ga)[16], int c0) {
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-              s += fast_exp2(fmaf(f[k] + g[k], c2, NL[c0 + k]));
+              s += fast_exp2(fmaf(__uint_as_float(fa[k]) + __uint_as_float(ga[k]), c2, NL[c0 + k]));
               if (++g_in == p.G) {
                 if (r < w.nrows && j < p.width) {
                   const bool v = (j < e.Sk) && (w.r0 + r < e.Sq) &&
@@ -992,6 +969,27 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
                 ++r;
               }
             }
+          };
+          const int n = p.n_mma;  // a multiple of 16
+          uint32_t fa[16], ga[16], fb[16], gb[16];
+          tmem_ld16_issue(taddr, fa);
+          tmem_ld16_issue(taddr + kHalfCols, ga);
+          tmem_ld_wait(fa, ga);
+          for (int c0 = 0; c0 < n; c0 += 32) {
+            const bool has_b = c0 + 16 < n;
+            const bool has_a = c0 + 32 < n;
+            if (has_b) {
+              tmem_ld16_issue(taddr + c0 + 16, fb);
+              tmem_ld16_issue(taddr + kHalfCols + c0 + 16, gb);
+            }
+            dense16(fa, ga, c0);
+            if (has_b) tmem_ld_wait(fb, gb);
+            if (has_a) {
+              tmem_ld16_issue(taddr + c0 + 32, fa);
+              tmem_ld16_issue(taddr + kHalfCols + c0 + 32, ga);
+            }
+            if (has_b) dense16(fb, gb, c0 + 16);
+            if (has_a) tmem_ld_wait(fa, ga);
           }
           tc_fence_before();
           mbar_arrive(bar_acc_empty + 8 * buf);
