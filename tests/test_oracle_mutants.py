@@ -162,12 +162,56 @@ def _mut_lse_mask_off(m):
     m.softmax_lse = f
 
 
+def _mut_bf16_read_as_fp16(m):
+    """bf16 bit patterns decoded as IEEE binary16"""
+    orig = m.decode_half
+    m.decode_half = lambda bits, dtype: orig(bits, "fp16")
+
+
+def _mut_minus_one_wraps(m):
+    """index -1 taken as the last key of the sequence (negative indexing)"""
+    orig = m.slot_valid
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
+        jj = np.where(j < 0, Sk - 1, j)
+        return orig(jj, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=topk_len)
+    m.slot_valid = f
+    orig_terms = m._row_terms
+    def terms(t, geo, qv, kv, dtype, sparse_indices, topk_length, width, mask_mode,
+              seqused_q=None, seqused_k=None):
+        q_row, sel_k, valid = orig_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length, width,
+                                         mask_mode, seqused_q, seqused_k)
+        if sparse_indices is not None:
+            b, r, Sq, k0, Sk = m._effective(geo[t], seqused_q, seqused_k)
+            idx_row = np.asarray(sparse_indices).reshape(len(geo), -1)[t].astype(np.int64)
+            neg = (idx_row < 0) & valid
+            if neg.any() and Sk > 0:
+                sel_k = sel_k.copy()
+                sel_k[neg] = m.decode_half(kv[k0 + Sk - 1], dtype)
+        return q_row, sel_k, valid
+    m._row_terms = terms
+
+
+def _mut_seqused_k_ignored(m):
+    orig = m._effective
+    m._effective = lambda g, sq, sk: orig(g, sq, None)
+
+
+def _mut_slots_in_key_order(m):
+    """sparse outputs written in ascending key order instead of slot order"""
+    orig = m.slot_key_positions
+    def f(idx_row, width):
+        j = orig(idx_row, width)
+        return np.sort(j) if idx_row is not None else j
+    m.slot_key_positions = f
+
+
 MUTANTS = [_mut_drop_scale, _mut_sign, _mut_sum_not_mean, _mut_divide_by_slots,
            _mut_causal_off_by_one, _mut_causal_top_left, _mut_ignore_topk_length,
            _mut_mask_on_slot, _mut_lse_head_order, _mut_tnd_key_offset,
            _mut_keep_out_of_range, _mut_log2, _mut_lse_no_scale, _mut_seqused_q_ignored,
            _mut_seqused_causal_full_lengths, _mut_lse_base2, _mut_lse_drops_topk_length,
-           _mut_lse_mask_off]
+           _mut_lse_mask_off, _mut_bf16_read_as_fp16, _mut_minus_one_wraps,
+           _mut_seqused_k_ignored, _mut_slots_in_key_order]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__[5:])
