@@ -327,6 +327,38 @@ smla_status smla_l1norm_schedule_host(const smla_l1norm_desc *desc, int32_t num_
 smla_status smla_debug_wait_timeout_probe(int64_t timeout_ns, smla_stream_t stream, int32_t *flags);
 
 /*
+ * Test hook: the key gather (stage 1 of the article's three-stage formula,
+ * selectedKv = Gather(K, sparse_indices)) alone, for one work item.  Runs the
+ * key-producer warps of a launch mode -- the same device code the operator
+ * runs -- over the work item of ``plan`` that holds query token ``token``,
+ * with one warp taking the place of the tensor cores: each 16 KB ring stage
+ * is copied to ``dump`` exactly as the MMA would read it, in stage order.
+ *
+ *   mode        0: the L1-norm launch's producers (two groups on alternate
+ *               stages); 1: the forward-LSE and fused launches' (one group).
+ *   dump        device buffer, 16-byte aligned, ``dump_bytes`` long.  Stage
+ *               n = 8*t + c holds head-dim columns 64c .. 64c+63 of the 128
+ *               key slots of key tile t: slot s of the tile (row s & 127) at
+ *               byte offset 16384*n + 128*s + 16*(p ^ (s & 7)) for its 16-byte
+ *               piece p (0..7) -- the 128-byte swizzle.  Stages beyond
+ *               dump_bytes / 16384 are not written.  The item's key tiles
+ *               are ceil(min(topk_length, topk) / 128) in the sparse form
+ *               (topk when there is no topk_length; 0 when the sequence has
+ *               no key), its precomputed tile count in the dense form.
+ *   k, sparse_indices, topk_length   as for smla_l1norm_run().
+ *
+ * A slot whose key position j is in [0, Sk) holds key row j of the token's
+ * sequence, bit for bit; any other slot (index -1 or out of range, slot
+ * past topk_length or topk) holds the sequence's key 0, which the epilogue
+ * masks to an output of 0.  Asynchronous on ``stream``; device flags go to
+ * the plan's status word.  Returns SMLA_ERR_INVALID for a bad mode, token or
+ * alignment, SMLA_ERR_NULLPTR for a missing pointer.
+ */
+smla_status smla_debug_gather(const smla_plan *plan, int32_t mode, int64_t token, const void *k,
+                              const int32_t *sparse_indices, const int32_t *topk_length, void *dump,
+                              int64_t dump_bytes, smla_stream_t stream);
+
+/*
  * Allocation-free form of smla_l1norm_run() (the article has no counterpart;
  * the operator is the same).  For callers that cannot call cudaMalloc: code
  * running where a framework's caching allocator owns all device memory, a
@@ -344,8 +376,12 @@ smla_status smla_debug_wait_timeout_probe(int64_t timeout_ns, smla_stream_t stre
  * The call allocates nothing: no cudaMalloc / cudaFree, no allocating CUDA
  * or torch routine, no host heap.  It builds the work list in fixed host
  * staging memory, copies it into the device array with cudaMemcpyAsync on
- * ``stream`` (from pageable memory, so the call waits for the stream's
- * earlier work before the copy starts), and launches the fused kernel.
+ * ``stream`` and launches the fused kernel.  The staging memory is pageable:
+ * the call returns once the copy has taken the host bytes, and the device
+ * copy is ordered after earlier work on ``stream``.  The launch shape (CTAs,
+ * key-ring depth, shared memory), the validation and the device-side wait
+ * limit (SMLA_WAIT_TIMEOUT_NS / SMLA_WAIT_TIMEOUT_MS) are the plan path's;
+ * smla_debug_noalloc_config() reports the shape without a GPU.
  *
  * Set-up: the first call on each device (with that device current) looks up
  * the device address of the scratch array with cudaGetSymbolAddress and
@@ -364,6 +400,20 @@ smla_status smla_debug_wait_timeout_probe(int64_t timeout_ns, smla_stream_t stre
 smla_status smla_l1norm_run_noalloc(const smla_l1norm_desc *desc, const void *q, const void *k,
                                     const float *softmax_lse, const int32_t *sparse_indices,
                                     const int32_t *topk_length, float *out, smla_stream_t stream);
+
+/*
+ * Host-only view of smla_l1norm_run_noalloc()'s launch shape, for tests (the
+ * article has no counterpart): validates ``desc`` exactly as that call does
+ * and fills ``info`` with what it would launch on a device with ``num_sms``
+ * SMs and ``smem_optin`` bytes of opt-in shared memory per block: num_ctas,
+ * stages (key-ring depth), smem_bytes, mma_n, rows_per_item, num_items,
+ * num_tokens, out_width and the q / k row counts; the cost fields are 0.
+ * No CUDA call.  Returns the validation codes, SMLA_ERR_CAPACITY for a
+ * problem beyond the fixed scratch, SMLA_ERR_NULLPTR for a NULL ``info`` and
+ * SMLA_ERR_INVALID for a non-positive ``num_sms`` or ``smem_optin``.
+ */
+smla_status smla_debug_noalloc_config(const smla_l1norm_desc *desc, int32_t num_sms, int32_t smem_optin,
+                                      smla_plan_info *info);
 
 /* Static description of a status code. */
 const char *smla_status_string(smla_status status);

@@ -26,7 +26,7 @@ __all__ = [
     "SMLA_OK", "SMLA_ERR_NULLPTR", "SMLA_ERR_INVALID", "SMLA_ERR_UNSUPPORTED", "SMLA_ERR_CUDA",
     "SMLA_ERR_TIMEOUT", "SMLA_WARN_BAD_INDEX", "SMLA_ERR_CAPACITY", "SmlaError", "Plan", "library",
     "library_path", "sparse_flash_mla_softmax_l1_norm", "schedule_host", "wait_timeout_probe",
-    "run_noalloc",
+    "run_noalloc", "noalloc_config",
 ]
 
 SMLA_OK, SMLA_ERR_NULLPTR, SMLA_ERR_INVALID, SMLA_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -130,6 +130,10 @@ def library():
     lib.smla_get_last_cuda_error.restype = ctypes.c_char_p
     lib.smla_l1norm_run_noalloc.argtypes = [ctypes.POINTER(_Desc), P, P, P, P, P, P, P]
     lib.smla_l1norm_run_noalloc.restype = I32
+    lib.smla_debug_gather.argtypes = [P, I32, I64, P, P, P, P, I64, P]
+    lib.smla_debug_gather.restype = I32
+    lib.smla_debug_noalloc_config.argtypes = [ctypes.POINTER(_Desc), I32, I32, ctypes.POINTER(PlanInfo)]
+    lib.smla_debug_noalloc_config.restype = I32
     lib.smla_debug_wait_timeout_probe.argtypes = [I64, P, ctypes.POINTER(I32)]
     lib.smla_debug_wait_timeout_probe.restype = I32
     _ = F32
@@ -344,6 +348,18 @@ class Plan:
         code = self._lib.smla_l1norm_run_from_host(self._h, *hp, *dp, _stream_handle(stream))
         _check(code, "smla_l1norm_run_from_host")
 
+    def debug_gather(self, token, k, dump, sparse_indices=None, topk_length=None, mode=0, stream=None):
+        """``smla_debug_gather``: the key producers alone for the work item of
+        query ``token``; ``dump`` (a uint8 CUDA tensor) receives the ring
+        stages as the tensor cores would read them."""
+        code = self._lib.smla_debug_gather(self._h, int(mode), int(token), _ptr(k, "k", required=False),
+                                           _ptr(sparse_indices, "sparse_indices", required=False),
+                                           _ptr(topk_length, "topk_length", required=False),
+                                           _ptr(dump, "dump"), int(dump.numel() * dump.element_size()),
+                                           _stream_handle(stream))
+        _check(code, "smla_debug_gather")
+        return dump
+
     def status(self, stream=None):
         """(code, flags) from ``smla_l1norm_get_status`` (synchronises)."""
         flags = ctypes.c_int32()
@@ -378,6 +394,19 @@ def run_noalloc(q, k, softmax_lse, out, sparse_indices=None, topk_length=None, s
     del keep
     _check(code, "smla_l1norm_run_noalloc")
     return out
+
+
+def noalloc_config(num_sms: int, smem_optin: int, **desc_kwargs) -> PlanInfo:
+    """``smla_debug_noalloc_config``: the launch shape ``run_noalloc`` would
+    use on a device with ``num_sms`` SMs and ``smem_optin`` bytes of opt-in
+    shared memory (host only, no CUDA call)."""
+    lib = library()
+    d, keep = _make_desc(**desc_kwargs)
+    info = PlanInfo()
+    code = lib.smla_debug_noalloc_config(ctypes.byref(d), int(num_sms), int(smem_optin), ctypes.byref(info))
+    del keep
+    _check(code, "smla_debug_noalloc_config")
+    return info
 
 
 _PLAN_CACHE = {}

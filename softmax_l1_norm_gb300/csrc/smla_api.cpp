@@ -38,22 +38,37 @@ constexpr int kDefaultSmemOptin = 232448;  // 227 KB, the sm_100-family opt-in l
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-struct Geometry {
-  bool sparse = false;
-  bool tnd = false;
-  int G = 0;
-  int R = 1;
-  int n_mma = 16;
-  int width = 0;
-  int64_t n_tokens = 0;
-  int64_t q_rows = 0;
-  int64_t k_rows = 0;
-  int batch = 0;
+// A validated description plus its per-sequence offsets and lengths.
+struct Geometry : smla::Shape {
   std::vector<int64_t> q0, sq, k0, sk;  // per sequence
 };
 
-// Checks every field of the description; fills the geometry on success.
 smla_status validate(const smla_l1norm_desc* d, Geometry* g) {
+  smla_status st = smla::check_desc(d, g);
+  if (st != SMLA_OK) return st;
+  for (int b = 0; b < g->batch; ++b) {
+    if (g->tnd) {
+      g->q0.push_back(d->cu_seqlens_q[b]);
+      g->sq.push_back(static_cast<int64_t>(d->cu_seqlens_q[b + 1]) - d->cu_seqlens_q[b]);
+      g->k0.push_back(d->cu_seqlens_k[b]);
+      g->sk.push_back(static_cast<int64_t>(d->cu_seqlens_k[b + 1]) - d->cu_seqlens_k[b]);
+    } else {
+      g->q0.push_back(static_cast<int64_t>(b) * d->max_seqlen_q);
+      g->sq.push_back(d->max_seqlen_q);
+      g->k0.push_back(static_cast<int64_t>(b) * d->max_seqlen_k);
+      g->sk.push_back(d->max_seqlen_k);
+    }
+  }
+  return SMLA_OK;
+}
+
+}  // namespace
+
+namespace smla {
+
+// Checks every field of the description ([SMLA] 参数说明 and 约束说明) and
+// derives the launch geometry.  Reads the host cu_seqlens arrays in TND.
+smla_status check_desc(const smla_l1norm_desc* d, Shape* g) {
   if (d == nullptr) return SMLA_ERR_NULLPTR;
   if (d->layout_q != SMLA_LAYOUT_BSND && d->layout_q != SMLA_LAYOUT_TND) return SMLA_ERR_INVALID;
   if (d->layout_k != d->layout_q) return SMLA_ERR_INVALID;  // layout_q must equal layout_k
@@ -61,7 +76,7 @@ smla_status validate(const smla_l1norm_desc* d, Geometry* g) {
   if (d->num_heads_k != 1) return SMLA_ERR_INVALID;                          // N2 only 1
   if (d->num_heads_q < 1 || d->num_heads_q > 128) return SMLA_ERR_INVALID;   // N1 in 1..128
   if (d->num_heads_q % d->num_heads_k != 0) return SMLA_ERR_INVALID;
-  if (d->head_dim != smla::kHeadDim) return SMLA_ERR_INVALID;                 // D only 512
+  if (d->head_dim != kHeadDim) return SMLA_ERR_INVALID;                      // D only 512
   if (d->mask_mode == 1 || d->mask_mode == 2) return SMLA_ERR_UNSUPPORTED;
   if (d->mask_mode != 0 && d->mask_mode != 3) return SMLA_ERR_INVALID;
   if (d->cmp_ratio < 1 || d->cmp_ratio > 128) return SMLA_ERR_INVALID;       // range 1..128
@@ -72,9 +87,12 @@ smla_status validate(const smla_l1norm_desc* d, Geometry* g) {
   if (d->has_topk_length && d->topk == 0) return SMLA_ERR_INVALID;  // topk_length needs indices
   if (d->num_ctas < 0) return SMLA_ERR_INVALID;
 
+  *g = Shape{};
   g->sparse = d->topk > 0;
   g->tnd = d->layout_q == SMLA_LAYOUT_TND;
   g->G = d->num_heads_q / d->num_heads_k;
+  g->R = g->sparse ? 1 : std::max(1, 128 / g->G);
+  g->n_mma = static_cast<int>(std::max<int64_t>(16, ceil_div(static_cast<int64_t>(g->R) * g->G, 16) * 16));
   if (g->tnd) {
     if (d->cu_seqlens_q == nullptr || d->cu_seqlens_k == nullptr) return SMLA_ERR_NULLPTR;
     if (d->batch_size < 0) return SMLA_ERR_INVALID;
@@ -85,11 +103,9 @@ smla_status validate(const smla_l1norm_desc* d, Geometry* g) {
     int64_t max_sk = 0;
     for (int b = 0; b < g->batch; ++b) {
       if (cq[b + 1] < cq[b] || ck[b + 1] < ck[b]) return SMLA_ERR_INVALID;
-      g->q0.push_back(cq[b]);
-      g->sq.push_back(cq[b + 1] - cq[b]);
-      g->k0.push_back(ck[b]);
-      g->sk.push_back(ck[b + 1] - ck[b]);
-      max_sk = std::max<int64_t>(max_sk, ck[b + 1] - ck[b]);
+      const int64_t sq = static_cast<int64_t>(cq[b + 1]) - cq[b];
+      max_sk = std::max<int64_t>(max_sk, static_cast<int64_t>(ck[b + 1]) - ck[b]);
+      g->n_items += g->sparse ? sq : ceil_div(sq, g->R);
     }
     g->n_tokens = cq[g->batch];
     g->k_rows = ck[g->batch];
@@ -102,23 +118,11 @@ smla_status validate(const smla_l1norm_desc* d, Geometry* g) {
   } else {
     if (d->batch_size < 0 || d->max_seqlen_q < 0 || d->max_seqlen_k < 0) return SMLA_ERR_INVALID;
     g->batch = d->batch_size;
-    const int64_t S1 = d->max_seqlen_q, S2 = d->max_seqlen_k;
-    for (int b = 0; b < g->batch; ++b) {
-      g->q0.push_back(b * S1);
-      g->sq.push_back(S1);
-      g->k0.push_back(b * S2);
-      g->sk.push_back(S2);
-    }
-    g->n_tokens = static_cast<int64_t>(g->batch) * S1;
-    g->k_rows = static_cast<int64_t>(g->batch) * S2;
-    g->width = g->sparse ? d->topk : static_cast<int>(S2);
+    g->n_tokens = static_cast<int64_t>(g->batch) * d->max_seqlen_q;
+    g->k_rows = static_cast<int64_t>(g->batch) * d->max_seqlen_k;
+    g->width = g->sparse ? d->topk : d->max_seqlen_k;
+    g->n_items = g->sparse ? g->n_tokens : static_cast<int64_t>(g->batch) * ceil_div(d->max_seqlen_q, g->R);
   }
-  if (g->sparse) {
-    g->R = 1;
-  } else {
-    g->R = std::max(1, 128 / g->G);
-  }
-  g->n_mma = static_cast<int>(std::max<int64_t>(16, ceil_div(static_cast<int64_t>(g->R) * g->G, 16) * 16));
   g->q_rows = g->n_tokens * g->G;
   // TMA coordinates are 32-bit; keep every row index representable.
   if (g->q_rows + 256 >= (int64_t{1} << 31) || g->k_rows + 256 >= (int64_t{1} << 31)) return SMLA_ERR_INVALID;
@@ -131,6 +135,12 @@ int visible_keys(int64_t r, int64_t Sq, int64_t Sk, int mask_mode) {
   if (mask_mode == 0) return static_cast<int>(Sk);
   return static_cast<int>(std::min<int64_t>(Sk, std::max<int64_t>(0, r + Sk - Sq + 1)));
 }
+
+}  // namespace smla
+
+namespace {
+
+using smla::visible_keys;
 
 struct Schedule {
   std::vector<WorkItem> items;       // grouped by CTA
@@ -222,27 +232,6 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
   return s;
 }
 
-// Deepest key ring that fits, with an even number of slots (the kernel's
-// barrier phases rely on it when several producer groups fill the ring).
-int stages_for(int n_mma, int smem_limit) {
-  int st = smla::kMaxStages;
-  while (st > smla::kMinStages && smla::smem_bytes_for(n_mma, st) > smem_limit) st -= 2;
-  return st;
-}
-
-uint32_t make_idesc(int dtype, int n_mma) {
-  // tcgen05 instruction descriptor, kind::f16: fp32 accumulator, A and B of
-  // the same 16-bit type, both K-major, M = 128, N = n_mma.
-  const uint32_t ab = dtype == SMLA_DTYPE_BF16 ? 1u : 0u;
-  uint32_t d = 0;
-  d |= 1u << 4;                                    // D format: f32
-  d |= ab << 7;                                    // A format
-  d |= ab << 10;                                   // B format
-  d |= static_cast<uint32_t>(n_mma >> 3) << 17;    // N / 8
-  d |= static_cast<uint32_t>(128 >> 4) << 24;      // M / 16
-  return d;
-}
-
 void fill_info(const Geometry& g, const Schedule& s, int num_ctas, int stages, int smem, smla_plan_info* info) {
   std::memset(info, 0, sizeof(*info));
   info->num_tokens = g.n_tokens;
@@ -260,33 +249,62 @@ void fill_info(const Geometry& g, const Schedule& s, int num_ctas, int stages, i
   info->k_rows_total = g.k_rows;
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+
+namespace smla {
+
+int stages_for(int n_mma, int smem_limit) {
+  int st = kMaxStages;
+  while (st > kMinStages && smem_bytes_for(n_mma, st) > smem_limit) st -= 2;
+  return st;
+}
+
+uint32_t make_idesc(int dtype, int n_mma) {
+  // tcgen05 instruction descriptor, kind::f16: fp32 accumulator, A and B of
+  // the same 16-bit type, both K-major, M = 128, N = n_mma.
+  const uint32_t ab = dtype == SMLA_DTYPE_BF16 ? 1u : 0u;
+  uint32_t d = 0;
+  d |= 1u << 4;                                    // D format: f32
+  d |= ab << 7;                                    // A format
+  d |= ab << 10;                                   // B format
+  d |= static_cast<uint32_t>(n_mma >> 3) << 17;    // N / 8
+  d |= static_cast<uint32_t>(128 >> 4) << 24;      // M / 16
+  return d;
+}
+
+namespace {
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  // resolved once (thread-safe static initialisation)
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return nullptr;
+  }();
   return fn;
 }
+
+}  // namespace
 
 // 2-D view (rows x 512) of a half-precision tensor, boxes of 64 columns x
 // box_rows rows, 128-byte swizzle (the layout the MMA descriptors expect).
 bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int box_rows, int dtype) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(smla::kHeadDim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(smla::kHeadDim) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(smla::kChunkElems), static_cast<cuuint32_t>(box_rows)};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkElems), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt =
       dtype == SMLA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -295,19 +313,20 @@ bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int box_ro
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
-
 int64_t wait_timeout_ns() {
-  const char* e = std::getenv("SMLA_WAIT_TIMEOUT_MS");
-  if (e != nullptr) {
+  if (const char* e = std::getenv("SMLA_WAIT_TIMEOUT_NS")) {
+    char* end = nullptr;
+    const long long ns = std::strtoll(e, &end, 10);
+    if (end != e && ns >= 0) return ns;
+  }
+  if (const char* e = std::getenv("SMLA_WAIT_TIMEOUT_MS")) {
     const long long ms = std::atoll(e);
     if (ms > 0) return ms * 1000000LL;
   }
   return 2000LL * 1000000LL;  // 2 s
 }
 
-}  // namespace
+}  // namespace smla
 
 struct smla_plan {
   smla_l1norm_desc desc;
@@ -323,6 +342,7 @@ struct smla_plan {
   WorkItem* d_items = nullptr;
   smla_plan_info info{};
   int64_t timeout_ns = 0;
+  std::vector<WorkItem> items_host;  // the work list as uploaded, for the gather test hook
   // run_from_host pipeline: token chunks, each with its own work schedule,
   // so that the copies of one chunk overlap the kernel of the previous one
   std::vector<int64_t> chunk_lo, chunk_hi;
@@ -361,7 +381,7 @@ smla_status smla_l1norm_schedule_host(const smla_l1norm_desc* desc, int32_t num_
   }
   if (cta_offsets != nullptr) std::memcpy(cta_offsets, s.cta_begin.data(), s.cta_begin.size() * sizeof(int32_t));
   if (info != nullptr) {
-    const int stages = stages_for(g.n_mma, kDefaultSmemOptin);
+    const int stages = smla::stages_for(g.n_mma, kDefaultSmemOptin);
     fill_info(g, s, num_ctas, stages, smla::smem_bytes_for(g.n_mma, stages), info);
   }
   return SMLA_OK;
@@ -380,8 +400,8 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   plan->desc.cu_seqlens_k = nullptr;
   plan->desc.topk_length_hint = nullptr;
   plan->geo = g;
-  plan->idesc = make_idesc(desc->dtype, g.n_mma);
-  plan->timeout_ns = wait_timeout_ns();
+  plan->idesc = smla::make_idesc(desc->dtype, g.n_mma);
+  plan->timeout_ns = smla::wait_timeout_ns();
 
   cudaError_t e = cudaGetDevice(&plan->device);
   if (e != cudaSuccess) {
@@ -398,7 +418,7 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   int ctas = desc->num_ctas > 0 ? desc->num_ctas : sms;
   ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(ctas, std::max<int64_t>(1, g.n_tokens))));
   plan->num_ctas = ctas;
-  plan->stages = stages_for(g.n_mma, optin);
+  plan->stages = smla::stages_for(g.n_mma, optin);
   plan->smem = smla::smem_bytes_for(g.n_mma, plan->stages);
   if (plan->smem > optin) {
     release_plan(plan);
@@ -406,6 +426,7 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   }
   const Schedule s = build_schedule(desc, g, ctas);
   fill_info(g, s, ctas, plan->stages, plan->smem, &plan->info);
+  plan->items_host = s.items;
 
   // Token chunks for run_from_host: cut the token-ordered work items into
   // kHostChunks runs of about equal token count (an item never straddles a
@@ -455,7 +476,7 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
       std::memcpy(host.data() + off_ci[c], cs[c].items.data(), cs[c].items.size() * sizeof(WorkItem));
   }
   e = cudaMemcpy(plan->dbuf, host.data(), bytes, cudaMemcpyHostToDevice);
-  if (e == cudaSuccess) e = smla::configure_fused(plan->smem);
+  if (e == cudaSuccess) e = smla::configure_fused_for_device();
   if (e == cudaSuccess && !cs.empty()) {
     e = cudaStreamCreateWithFlags(&plan->s_in, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&plan->s_out, cudaStreamNonBlocking);
@@ -562,7 +583,7 @@ smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, flo
 
   CUtensorMap tq;
   const int q_box = g.R * g.G;
-  if (!encode_rows_map(&tq, t->q, g.q_rows, q_box, plan->desc.dtype)) {
+  if (!smla::encode_rows_map(&tq, t->q, g.q_rows, q_box, plan->desc.dtype)) {
     g_last_cuda_error = "cuTensorMapEncodeTiled(q) failed";
     return SMLA_ERR_CUDA;
   }
@@ -587,7 +608,7 @@ smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, flo
   p.mask_mode = plan->desc.mask_mode;
   p.stages = plan->stages;
   p.idesc = static_cast<int32_t>(plan->idesc);
-  p.idesc_lse = static_cast<int32_t>(make_idesc(plan->desc.dtype, smla::kTileKeys));
+  p.idesc_lse = static_cast<int32_t>(smla::make_idesc(plan->desc.dtype, smla::kTileKeys));
   p.c_log2 = static_cast<float>(static_cast<double>(plan->desc.softmax_scale) * 1.4426950408889634);
   p.inv_g = 1.0f / static_cast<float>(g.G);
   p.timeout_ns = plan->timeout_ns;
@@ -739,6 +760,50 @@ smla_status smla_debug_wait_timeout_probe(int64_t timeout_ns, smla_stream_t stre
   if (e != cudaSuccess) return cuda_fail(e, "wait probe");
   if (flags != nullptr) *flags = v;
   return (v & smla::kFlagTimeout) ? SMLA_ERR_TIMEOUT : SMLA_OK;
+}
+
+smla_status smla_debug_gather(const smla_plan* plan, int32_t mode, int64_t token, const void* k,
+                              const int32_t* sparse_indices, const int32_t* topk_length, void* dump,
+                              int64_t dump_bytes, smla_stream_t stream) {
+  if (plan == nullptr || dump == nullptr) return SMLA_ERR_NULLPTR;
+  if (mode != smla::kModeL1 && mode != smla::kModeLse) return SMLA_ERR_INVALID;
+  const Geometry& g = plan->geo;
+  if (token < 0 || token >= g.n_tokens) return SMLA_ERR_INVALID;
+  if (g.k_rows > 0 && k == nullptr) return SMLA_ERR_NULLPTR;
+  if (g.sparse && sparse_indices == nullptr) return SMLA_ERR_NULLPTR;
+  if (plan->desc.has_topk_length && topk_length == nullptr) return SMLA_ERR_NULLPTR;
+  if ((k != nullptr && !aligned16(k)) || !aligned16(dump)) return SMLA_ERR_INVALID;
+  int item = -1;
+  for (size_t i = 0; i < plan->items_host.size(); ++i) {
+    const WorkItem& w = plan->items_host[i];
+    if (token >= w.q_tok && token < static_cast<int64_t>(w.q_tok) + w.nrows) {
+      item = static_cast<int>(i);
+      break;
+    }
+  }
+  if (item < 0) return SMLA_ERR_INVALID;
+  smla::KernelParams p{};
+  p.k = static_cast<const uint8_t*>(k);
+  p.items = plan->d_items;
+  p.cta_begin = plan->d_cta_begin;
+  p.status = plan->d_status;
+  p.idx = g.sparse ? sparse_indices : nullptr;
+  p.topk_len = plan->desc.has_topk_length ? topk_length : nullptr;
+  p.G = g.G;
+  p.R = g.R;
+  p.n_mma = g.n_mma;
+  p.q_box_rows = g.R * g.G;
+  p.topk = g.sparse ? plan->desc.topk : 0;
+  p.width = g.width;
+  p.mask_mode = plan->desc.mask_mode;
+  p.stages = plan->stages;
+  p.timeout_ns = plan->timeout_ns;
+  cudaError_t e = smla::configure_fused_for_device();
+  if (e == cudaSuccess)
+    e = smla::launch_gather_dump(p, g.sparse, mode, item, item + 1, static_cast<uint8_t*>(dump),
+                                 dump_bytes / smla::kKStageBytes, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gather dump");
+  return SMLA_OK;
 }
 
 const char* smla_status_string(smla_status s) {

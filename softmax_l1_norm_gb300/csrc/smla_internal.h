@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/smla_l1norm.h"
+
 namespace smla {
 
 // Head dimension fixed by the operator's constraints (D = 512).
@@ -96,6 +98,52 @@ enum Mode : int {
 // Launch the fused kernel (defined in smla_kernel.cu).
 cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int mode, int grid,
                          int smem_bytes, cudaStream_t stream);
-cudaError_t configure_fused(int smem_bytes);
+// Raise every instantiation's dynamic shared-memory cap to the current
+// device's opt-in maximum, once per device (smla_kernel.cu).  The cap only
+// ever rises, so a plan built for a small footprint never lowers it under
+// another plan's larger one.
+cudaError_t configure_fused_for_device();
+// Test hook: the key producers of a launch mode (kModeL1 or kModeLse) alone
+// over work items [it0, it1), each ring stage copied to ``dump`` as the MMA
+// would read it (smla_kernel.cu).  One CTA.
+cudaError_t launch_gather_dump(const KernelParams& p, bool sparse, int mode, int it0, int it1, uint8_t* dump,
+                               int64_t max_stages, cudaStream_t stream);
+
+// ---------------------------------------------------------------- host side
+// Shared by the plan path (smla_api.cpp) and the allocation-free path
+// (smla_noalloc.cu); none of these allocates memory of any kind.
+
+// What a description asks for, once validated.
+struct Shape {
+  bool sparse = false;
+  bool tnd = false;
+  int G = 0;
+  int R = 1;        // tokens packed per MMA (dense form), 1 (sparse)
+  int n_mma = 16;   // MMA N: R*G padded to 16
+  int width = 0;    // output row length
+  int batch = 0;
+  int64_t n_tokens = 0;
+  int64_t q_rows = 0;   // rows of the 2-D (tokens*G) x 512 view of q
+  int64_t k_rows = 0;
+  int64_t n_items = 0;  // work items: tokens (sparse) or packs of R tokens of one sequence (dense)
+};
+
+// Every check of the article's parameter tables and constraints on a
+// description; fills ``s`` on success.  No CUDA call.
+smla_status check_desc(const smla_l1norm_desc* d, Shape* s);
+// Keys of a sequence visible from local row r (mask_mode 3), or all of them.
+int visible_keys(int64_t r, int64_t Sq, int64_t Sk, int mask_mode);
+// Deepest key ring that fits in ``smem_limit`` bytes with an even number of
+// stages, at least kMinStages (the barrier phases rely on it when several
+// producer groups fill the ring).
+int stages_for(int n_mma, int smem_limit);
+// tcgen05 instruction descriptor, kind::f16, M = 128, N = n_mma.
+uint32_t make_idesc(int dtype, int n_mma);
+// 2-D (rows x 512) SWIZZLE_128B tensor map of a half-precision tensor, boxes
+// of 64 columns x box_rows rows.
+bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int box_rows, int dtype);
+// Bound on every device-side wait: SMLA_WAIT_TIMEOUT_NS (nanoseconds, 0
+// allowed) or SMLA_WAIT_TIMEOUT_MS, else 2 s.
+int64_t wait_timeout_ns();
 
 }  // namespace smla

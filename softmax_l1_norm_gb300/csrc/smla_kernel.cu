@@ -51,6 +51,7 @@
 // TMEM allocation is released.
 
 #include <cstdint>
+#include <mutex>
 
 #include "smla_internal.h"
 
@@ -529,6 +530,85 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
   }
 }
 
+// ---------------------------------------------------------------- key producers
+// Producer warp pw of group grp, lane l copies 16-byte segment (l & 7)
+// of key rows r0 + (l >> 3) + 4*i, i < keys_per_lane, of each of its
+// group's stages (4 whole 128-byte rows per warp instruction), r0 =
+// (pw % group_warps) * 128 / group_warps.  Stage n uses ring slot
+// n % stages.  Each lane's copies arrive on the slot's full barrier by
+// themselves when they land (cp.async.mbarrier.arrive.noinc), so a
+// producer only waits for free slots.  The generic-to-async proxy fence
+// the tensor cores need is executed by the MMA thread after it acquires
+// the full barrier: in a producer it would also wait for the copies
+// still in flight.
+template <bool kSparse, int kMode>
+__device__ __forceinline__ void produce_keys(const KernelParams& p, int pw, int lane, uint32_t sK,
+                                             uint32_t bar_k_full, uint32_t bar_k_empty, const WaitCtl& ctl,
+                                             int it0, int it1) {
+  constexpr int kGW = group_warps<kMode>();
+  constexpr int kKeysPerLane = keys_per_lane<kMode>();
+  const int grp = pw / kGW;
+  const int seg = lane & 7;
+  const int krow0 = (pw % kGW) * (kTileKeys / kGW) + (lane >> 3);
+  const uint32_t S = static_cast<uint32_t>(p.stages);
+  constexpr uint32_t kStep = producer_groups<kMode>();  // chunks between this group's stages
+  uint32_t kst = grp, kph = 0;  // slot of this group's next stage and its phase (S >= kStep)
+  bool ok = true;
+  TileCursor cur{it0 - 1, 0, 0, 0, 0, WorkItem{}};
+  bool have = cursor_next<kSparse, kMode>(p, cur, it1);
+  int jn[kKeysPerLane];
+  auto fetch_indices = [&](const TileCursor& c) {
+#pragma unroll
+    for (int i = 0; i < kKeysPerLane; ++i) {
+      const int slot = c.ktile() * kTileKeys + krow0 + 4 * i;
+      if (kSparse) {
+        jn[i] = slot < c.tl ? __ldg(p.idx + static_cast<int64_t>(c.w.q_tok) * p.topk + slot) : -1;
+      } else {
+        jn[i] = slot;
+      }
+    }
+  };
+  if (have) fetch_indices(cur);
+  const uint8_t* kseg = p.k + seg * 16;
+  while (have && ok) {
+    // source key rows of this tile (invalid slots read key 0 of the sequence)
+    int64_t row[kKeysPerLane];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kKeysPerLane; ++i) {
+      const int j = jn[i];
+      const bool in = (j >= 0) && (j < cur.w.Sk);
+      if (kSparse) bad |= (krow0 + 4 * i + cur.ktile() * kTileKeys < cur.tl) && !in && (j != -1);
+      row[i] = static_cast<int64_t>(cur.w.k_base) + (in ? j : 0);
+    }
+    if (kSparse && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kFlagBadIndex);
+    TileCursor nxt = cur;
+    const bool have_next = cursor_next<kSparse, kMode>(p, nxt, it1);
+    if (have_next) fetch_indices(nxt);  // in flight while this tile streams
+    for (int c = grp; c < kNumChunks; c += kStep) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bar_k_empty + 8 * kst, kph ^ 1u, ctl));
+      if (!ok) break;
+      const uint32_t dst = sK + kst * kKStageBytes;
+      const uint8_t* kc = kseg + c * (kChunkElems * 2);
+#pragma unroll
+      for (int i = 0; i < kKeysPerLane; ++i) {
+        const int r = krow0 + 4 * i;
+        cp_async_16(dst + r * 128 + ((seg ^ (r & 7)) << 4), kc + row[i] * (kHeadDim * 2));
+      }
+      cp_async_arrive_noinc(bar_k_full + 8 * kst);
+      kst += kStep;
+      if (kst >= S) {
+        kst -= S;
+        kph ^= 1u;
+      }
+    }
+    cur = nxt;
+    have = have_next;
+  }
+  // Copies still in flight land before shared memory is released.
+  cp_async_wait_all();
+}
+
 }  // namespace
 
 template <bool kSparse, int kMode>
@@ -607,78 +687,7 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
   const int pw = producer_index<kMode>(warp);
   if (pw >= 0) {
     // ============================================================ key producers
-    // Producer warp pw of group grp, lane l copies 16-byte segment (l & 7)
-    // of key rows r0 + (l >> 3) + 4*i, i < keys_per_lane, of each of its
-    // group's stages (4 whole 128-byte rows per warp instruction), r0 =
-    // (pw % group_warps) * 128 / group_warps.  Stage n uses ring slot
-    // n % stages.  Each lane's copies arrive on the slot's full barrier by
-    // themselves when they land (cp.async.mbarrier.arrive.noinc), so a
-    // producer only waits for free slots.  The generic-to-async proxy fence
-    // the tensor cores need is executed by the MMA thread after it acquires
-    // the full barrier: in a producer it would also wait for the copies
-    // still in flight.
-    constexpr int kGW = group_warps<kMode>();
-    constexpr int kKeysPerLane = keys_per_lane<kMode>();
-    const int grp = pw / kGW;
-    const int seg = lane & 7;
-    const int krow0 = (pw % kGW) * (kTileKeys / kGW) + (lane >> 3);
-    const uint32_t S = static_cast<uint32_t>(p.stages);
-    constexpr uint32_t kStep = producer_groups<kMode>();  // chunks between this group's stages
-    uint32_t kst = grp, kph = 0;  // slot of this group's next stage and its phase (S >= kStep)
-    bool ok = true;
-    TileCursor cur{it0 - 1, 0, 0, 0, 0, WorkItem{}};
-    bool have = cursor_next<kSparse, kMode>(p, cur, it1);
-    int jn[kKeysPerLane];
-    auto fetch_indices = [&](const TileCursor& c) {
-#pragma unroll
-      for (int i = 0; i < kKeysPerLane; ++i) {
-        const int slot = c.ktile() * kTileKeys + krow0 + 4 * i;
-        if (kSparse) {
-          jn[i] = slot < c.tl ? __ldg(p.idx + static_cast<int64_t>(c.w.q_tok) * p.topk + slot) : -1;
-        } else {
-          jn[i] = slot;
-        }
-      }
-    };
-    if (have) fetch_indices(cur);
-    const uint8_t* kseg = p.k + seg * 16;
-    while (have && ok) {
-      // source key rows of this tile (invalid slots read key 0 of the sequence)
-      int64_t row[kKeysPerLane];
-      bool bad = false;
-#pragma unroll
-      for (int i = 0; i < kKeysPerLane; ++i) {
-        const int j = jn[i];
-        const bool in = (j >= 0) && (j < cur.w.Sk);
-        if (kSparse) bad |= (krow0 + 4 * i + cur.ktile() * kTileKeys < cur.tl) && !in && (j != -1);
-        row[i] = static_cast<int64_t>(cur.w.k_base) + (in ? j : 0);
-      }
-      if (kSparse && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kFlagBadIndex);
-      TileCursor nxt = cur;
-      const bool have_next = cursor_next<kSparse, kMode>(p, nxt, it1);
-      if (have_next) fetch_indices(nxt);  // in flight while this tile streams
-      for (int c = grp; c < kNumChunks; c += kStep) {
-        ok = __all_sync(0xffffffffu, wait_bounded(bar_k_empty + 8 * kst, kph ^ 1u, ctl));
-        if (!ok) break;
-        const uint32_t dst = sK + kst * kKStageBytes;
-        const uint8_t* kc = kseg + c * (kChunkElems * 2);
-#pragma unroll
-        for (int i = 0; i < kKeysPerLane; ++i) {
-          const int r = krow0 + 4 * i;
-          cp_async_16(dst + r * 128 + ((seg ^ (r & 7)) << 4), kc + row[i] * (kHeadDim * 2));
-        }
-        cp_async_arrive_noinc(bar_k_full + 8 * kst);
-        kst += kStep;
-        if (kst >= S) {
-          kst -= S;
-          kph ^= 1u;
-        }
-      }
-      cur = nxt;
-      have = have_next;
-    }
-    // Copies still in flight land before shared memory is released.
-    cp_async_wait_all();
+    produce_keys<kSparse, kMode>(p, pw, lane, sK, bar_k_full, bar_k_empty, ctl, it0, it1);
   } else if (warp == kQWarp) {
     // ============================================================ q loader
     if (lane == 0) {
@@ -1040,18 +1049,120 @@ __global__ void smla_wait_timeout_probe_kernel(int32_t* status, int64_t timeout_
   if (threadIdx.x == 0) mbar_arrive(smem_u32(&bar));
 }
 
-cudaError_t configure_fused(int smem_bytes) {
+// Test hook: the key producers of one launch mode, alone, over the work
+// items [it0, it1) of a schedule, running the same produce_keys code as the
+// fused kernel.  Warp 0 stands in for the MMA issuers: it takes the ring
+// stages in order (stage n = chunk n % 8 of key tile n / 8, in ring slot
+// n % stages), copies each 16 KB stage to ``dump`` exactly as it sits in
+// shared memory (128 key rows of 128 bytes, 16-byte pieces in the 128-byte
+// swizzle) and frees the slot.  Stages past ``max_stages`` are consumed
+// without being written.
+template <bool kSparse, int kMode>
+__global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
+    smla_gather_dump_kernel(const __grid_constant__ KernelParams p, int it0, int it1, uint8_t* dump,
+                            int64_t max_stages) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sK = base;
+  const uint32_t bar_k_full = sK + p.stages * kKStageBytes;
+  const uint32_t bar_k_empty = bar_k_full + 8 * kMaxStages;
+  volatile int32_t* abort_flag =
+      reinterpret_cast<volatile int32_t*>(gbase + (bar_k_empty + 8 * kMaxStages - base));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(bar_k_full + 8 * s, group_warps<kMode>() * 32);
+      mbar_init(bar_k_empty + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int pw = producer_index<kMode>(warp);
+  if (pw >= 0) {
+    produce_keys<kSparse, kMode>(p, pw, lane, sK, bar_k_full, bar_k_empty, ctl, it0, it1);
+  } else if (warp == 0) {
+    const int64_t S = p.stages;
+    TileCursor cur{it0 - 1, 0, 0, 0, 0, WorkItem{}};
+    int64_t n = 0;
+    bool ok = true;
+    while (ok && cursor_next<kSparse, kMode>(p, cur, it1)) {
+      for (int c = 0; c < kNumChunks; ++c, ++n) {
+        const uint32_t slot = static_cast<uint32_t>(n % S);
+        const uint32_t ph = static_cast<uint32_t>((n / S) & 1);
+        // every lane acquires the stage, so every lane's reads see the copies
+        ok = __all_sync(0xffffffffu, wait_bounded(bar_k_full + 8 * slot, ph, ctl));
+        if (!ok) break;
+        if (n < max_stages) {
+          const uint4* src = reinterpret_cast<const uint4*>(gbase + (sK + slot * kKStageBytes - base));
+          uint4* dst = reinterpret_cast<uint4*>(dump + n * kKStageBytes);
+          for (int i = lane; i < kKStageBytes / 16; i += 32) dst[i] = src[i];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_k_empty + 8 * slot);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+int gather_dump_smem_bytes(int stages) { return 1024 + stages * kKStageBytes + 2 * kMaxStages * 8 + 64; }
+
+cudaError_t launch_gather_dump(const KernelParams& p, bool sparse, int mode, int it0, int it1, uint8_t* dump,
+                               int64_t max_stages, cudaStream_t stream) {
+  const int smem = gather_dump_smem_bytes(p.stages);
+  if (mode == kModeL1) {
+    const dim3 b(kernel_threads<kModeL1>());
+    if (sparse)
+      smla_gather_dump_kernel<true, kModeL1><<<1, b, smem, stream>>>(p, it0, it1, dump, max_stages);
+    else
+      smla_gather_dump_kernel<false, kModeL1><<<1, b, smem, stream>>>(p, it0, it1, dump, max_stages);
+  } else if (mode == kModeLse) {
+    const dim3 b(kernel_threads<kModeLse>());
+    if (sparse)
+      smla_gather_dump_kernel<true, kModeLse><<<1, b, smem, stream>>>(p, it0, it1, dump, max_stages);
+    else
+      smla_gather_dump_kernel<false, kModeLse><<<1, b, smem, stream>>>(p, it0, it1, dump, max_stages);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t configure_fused_for_device() {
+  // Once per device, every instantiation's cap goes to the opt-in maximum;
+  // a launch still asks for exactly the shared memory its plan needs.
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static bool done[kMaxDevices] = {};
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
   const void* fns[] = {
       reinterpret_cast<const void*>(smla_fused_kernel<true, kModeL1>),
       reinterpret_cast<const void*>(smla_fused_kernel<false, kModeL1>),
       reinterpret_cast<const void*>(smla_fused_kernel<true, kModeLse>),
       reinterpret_cast<const void*>(smla_fused_kernel<false, kModeLse>),
       reinterpret_cast<const void*>(smla_fused_kernel<true, kModeFused>),
-      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeFused>)};
+      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeFused>),
+      reinterpret_cast<const void*>(smla_gather_dump_kernel<true, kModeL1>),
+      reinterpret_cast<const void*>(smla_gather_dump_kernel<false, kModeL1>),
+      reinterpret_cast<const void*>(smla_gather_dump_kernel<true, kModeLse>),
+      reinterpret_cast<const void*>(smla_gather_dump_kernel<false, kModeLse>)};
   for (const void* f : fns) {
-    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e != cudaSuccess) return e;
   }
+  done[dev] = true;
   return cudaSuccess;
 }
 

@@ -129,13 +129,14 @@ def test_schedule_covers_every_token_once(G, topk, mask, layout):
     assert info.smem_bytes <= 232448 and 4 <= info.stages <= 12
 
 
-def test_key_ring_depth_is_even_for_every_head_count():
+@pytest.mark.parametrize("topk", [256, 0])
+def test_key_ring_depth_is_even_for_every_head_count(topk):
     """The key ring always has an even number of stages, at least 4: with two
     producer groups filling alternate stages, an odd depth would let an MMA
-    issuer test a stage's full barrier two phases early."""
+    issuer test a stage's full barrier two phases early.  Sparse and dense."""
     for G in range(1, 129):
         _, _, info = smla.schedule_host(152, want_items=False, num_heads_q=G, batch_size=1,
-                                        max_seqlen_q=64, max_seqlen_k=512, topk=256, mask_mode=3,
+                                        max_seqlen_q=64, max_seqlen_k=512, topk=topk, mask_mode=3,
                                         has_topk_length=False, softmax_scale=0.05)
         assert info.stages % 2 == 0 and 4 <= info.stages <= 12, (G, info.stages)
         assert info.smem_bytes <= 232448

@@ -237,19 +237,65 @@ def test_wait_timeout_probe_reports_and_returns(lib):
     assert float(x.sum()) == 4.0
 
 
+def test_fused_kernel_waits_give_up_and_report(lib, monkeypatch):
+    """A plan made with a device wait limit of 0 ns: the first wait of the
+    fused kernel that is not already satisfied gives up, sets the CTA's abort
+    flag and the timeout bit; every role leaves its loop, copies and MMAs in
+    flight are drained and TMEM is released.  Each launch mode reports
+    SMLA_ERR_TIMEOUT, and afterwards the context still computes the oracle's
+    result with a normal plan."""
+    w = W.make_workload(layout="BSND", dtype="bf16", B=1, S1=64, S2=2500, G=128, topk=2048, mask_mode=3,
+                        seed=5200, lse=None)
+    exact_lse(oracle, w)
+    t = to_device(w)
+    monkeypatch.setenv("SMLA_WAIT_TIMEOUT_NS", "0")
+    plan0 = lib.Plan(**plan_kwargs(w))
+    monkeypatch.delenv("SMLA_WAIT_TIMEOUT_NS")
+    runs = {
+        "l1": lambda: plan0.run(t["q"], t["k"], t["lse"], sparse_indices=t["idx"], topk_length=t["tl"]),
+        "lse": lambda: plan0.softmax_lse(t["q"], t["k"], sparse_indices=t["idx"], topk_length=t["tl"]),
+        "fused": lambda: plan0.run_fused_lse(t["q"], t["k"], sparse_indices=t["idx"], topk_length=t["tl"]),
+    }
+    for name, fn in runs.items():
+        fn()
+        torch.cuda.synchronize()
+        code, flags = plan0.status()
+        assert code == lib.SMLA_ERR_TIMEOUT and (flags & 2), (name, code, flags)
+    got, plan, _, status = run_gpu(lib, w, tensors=t)
+    assert status[0] == lib.SMLA_OK
+    want = oracle.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **oracle_kwargs(w))
+    assert_close(got, want, what="normal plan after the aborted launches")
+
+
 # ---------------------------------------------------------------- full sizes
+def rows_from_every_cta(lib, w, plan, rng):
+    """One query token from each CTA's item list of ``plan``'s schedule (the
+    host scheduler builds the same list for the same description and grid)."""
+    items, offs, _ = lib.schedule_host(plan.info.num_ctas, **plan_kwargs(w))
+    rows = []
+    for c in range(len(offs) - 1):
+        if offs[c + 1] > offs[c]:
+            it = items[int(rng.integers(offs[c], offs[c + 1]))]
+            rows.append(int(it[0]) + int(rng.integers(0, it[1])))
+    return rows
+
+
 def sampled_parity(lib, n, n_sample=24, seed=0):
     """Full-size configuration, in the launch configuration the benchmark
-    times.  Exact LSE is planted for a sample of rows, which are compared
-    element by element with the oracle and must sum to 1; every row is
-    checked for exact zeros on invalid slots and for finite, non-negative
-    values."""
+    times.  Exact LSE is planted for a sample of rows -- one from every CTA's
+    share of the schedule plus random ones -- which are compared element by
+    element with the oracle and must sum to 1; every row is checked for exact
+    zeros on invalid slots and for finite, non-negative values."""
     w = W.make_config(n)
     rng = np.random.Generator(np.random.PCG64(seed))
     n_tok = w.n_tokens
-    rows = sorted(set([0, 1, n_tok - 1, n_tok // 2] + rng.choice(n_tok, n_sample, replace=False).tolist()))
+    plan = lib.Plan(**plan_kwargs(w))
+    rows = set([0, 1, n_tok - 1, n_tok // 2] + rng.choice(n_tok, n_sample, replace=False).tolist())
+    per_cta = rows_from_every_cta(lib, w, plan, rng)
+    assert len(per_cta) == plan.info.num_ctas
+    rows = sorted(rows | set(per_cta))
     exact_lse(oracle, w, rows=rows)
-    got, plan, t, status = run_gpu(lib, w)
+    got, plan, t, status = run_gpu(lib, w, plan=plan)
     assert status[0] == lib.SMLA_OK
     got_rows = got.reshape(n_tok, -1)
     want = oracle.softmax_l1_norm_rows(w.q_bits, w.k_bits, w.softmax_lse, rows, **oracle_kwargs(w))
@@ -262,8 +308,23 @@ def sampled_parity(lib, n, n_sample=24, seed=0):
     return w, got_rows
 
 
-def test_config3_dsv32_full_size_sampled(lib):
-    sampled_parity(lib, 3)
+def test_config3_dsv32_full_size_every_row(lib, tmp_path):
+    """The 4096-token, 128-head, top-2048 causal workload at full size, in the
+    benchmark's launch configuration: the exact forward LSE is planted on
+    every row and every one of the 8.4 M output elements is compared with the
+    oracle; every row sums to 1 within 1e-3 and masked slots are exactly 0."""
+    import oracle_pool
+    w = W.make_config(3)
+    n_tok = w.n_tokens
+    lse, want = oracle_pool.lse_and_rows(w, range(n_tok), str(tmp_path / "c3"))
+    W.set_lse_rows(w, lse)
+    got, plan, t, status = run_gpu(lib, w)
+    assert status[0] == lib.SMLA_OK and plan.info.num_ctas == torch.cuda.get_device_properties(0).multi_processor_count
+    got_rows = got.reshape(n_tok, -1)
+    assert_close(got_rows, want, what="config 3, every element")
+    sums = got_rows.astype(np.float64).sum(axis=1)
+    assert np.all(np.abs(sums - 1.0) <= ROWSUM_TOL), (sums.min(), sums.max())
+    assert np.all(got_rows[invalid_slot_mask(w)] == 0.0)
 
 
 def test_config4_varlen_tnd_full_size_sampled(lib):

@@ -56,3 +56,22 @@ def test_config_geometry():
     w = W.make_config(2)
     assert w.out_shape() == (2, 512, 1, 512) and w.sparse_indices is None
     assert w.valid_slot_count() == 2 * 512 * 513 // 2
+
+
+def test_oracle_pool_equals_direct_oracle_calls(tmp_path):
+    """The process-pool helper of the full-size parity test returns exactly
+    what the oracle's functions return when called directly."""
+    import oracle
+    import oracle_pool
+    w = W.make_workload(layout="TND", dtype="fp16", seqlens_q=[5, 0, 9], seqlens_k=[40, 3, 300], G=4,
+                        topk=64, mask_mode=3, seed=77)
+    rows = [13, 0, 4, 5]
+    lse, out = oracle_pool.lse_and_rows(w, rows, str(tmp_path / "w"), processes=2, chunk=3)
+    kw = dict(dtype=w.dtype, sparse_indices=w.sparse_indices, topk_length=w.topk_length,
+              cu_seqlens_q=w.cu_seqlens_q, cu_seqlens_k=w.cu_seqlens_k, softmax_scale=w.softmax_scale,
+              max_seqlen_k=w.max_seqlen_k, mask_mode=w.mask_mode, layout=w.layout)
+    lse_d = oracle.softmax_lse(w.q_bits, w.k_bits, rows=rows, **kw).astype(np.float32)
+    assert np.array_equal(lse, lse_d)
+    full = np.zeros((w.n_tokens, w.G), np.float32)
+    full[rows] = lse_d
+    assert np.array_equal(out, oracle.softmax_l1_norm_rows(w.q_bits, w.k_bits, full, rows, **kw))
