@@ -34,14 +34,19 @@ import workloads as W  # noqa: E402
 
 METRIC = "selected q.k pairs/s (Softmax-L1Norm forward, whole job)"
 UNIT = "pairs/s"
-L2_FLUSH_BYTES = 512 << 20
+L2_FLUSH_BYTES = 512 << 20   # > the 129 MB L2
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "smla_fused_kernel_dsv32_traffic.txt")
 KERNEL_SRC = os.path.join(ROOT, "softmax_l1_norm_gb300", "csrc", "smla_kernel.cu")
 
 
 # ----------------------------------------------------------------------------
 def workload_numbers(w):
-    """Pairs, FLOPs and algorithmic bytes of one pass over the workload."""
+    """Pairs, FLOPs and bytes of one pass over the workload.
+
+    ``bytes_`` counts every gathered key row as read (the roofline the work
+    was specified against); ``compulsory`` counts each tensor once -- the
+    keys any slot refers to, q, the LSE, the indices and the output -- which
+    is what a pass must move between HBM and the chip at the least."""
     valid = w.valid_slot_count()
     pairs = valid * w.G
     flops = 2 * w.head_dim * pairs
@@ -54,7 +59,35 @@ def workload_numbers(w):
         "indices": 0 if w.sparse_indices is None else n * w.topk * 4,
         "topk_length": 0 if w.topk_length is None else n * 4,
     }
-    return pairs, flops, bytes_
+    compulsory = dict(bytes_)
+    compulsory.pop("k_gathered")
+    compulsory["k_unique"] = unique_key_rows(w) * w.head_dim * 2
+    return pairs, flops, bytes_, compulsory
+
+
+def unique_key_rows(w):
+    """Key rows that at least one kept slot refers to."""
+    tab = w.token_table()
+    n_rows = int(w.k_bits.reshape(-1, w.head_dim).shape[0])
+    if n_rows == 0:
+        return 0
+    seen = np.zeros(n_rows, dtype=bool)
+    if w.sparse_indices is None:
+        vis = W.visible_count(tab[:, 1], tab[:, 2], tab[:, 4], w.mask_mode)
+        vis = np.minimum(vis, w.out_width)
+        for b, q0, Sq, k0, Sk in w.sequences():
+            if Sq > 0:
+                seen[k0:k0 + int(vis[q0:q0 + Sq].max())] = True
+        return int(seen.sum())
+    idx = w.sparse_indices.reshape(w.n_tokens, w.topk).astype(np.int64)
+    Sk = tab[:, 4:5]
+    ok = (idx >= 0) & (idx < Sk)
+    if w.mask_mode == 3:
+        ok &= idx <= (tab[:, 1:2] + Sk - tab[:, 2:3])
+    if w.topk_length is not None:
+        ok &= np.arange(w.topk)[None, :] < w.topk_length.reshape(w.n_tokens, 1).astype(np.int64)
+    seen[(tab[:, 3:4] + idx)[ok]] = True
+    return int(seen.sum())
 
 
 def load_peaks():
@@ -313,21 +346,75 @@ def run_reference(args, world, rank):
     return 0
 
 
-def run_ours(args, world, rank, local):
+class L2Flush:
+    """Between timed launches: write 512 MB (evicts all of the 129 MB L2),
+    then read a separate 256 MB buffer, so that the lines the write left
+    dirty are written back to HBM here and not charged to the next timed
+    launch.  The timed kernel starts with none of its data in L2."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=device)
+        self.acc = torch.empty((), dtype=torch.float32, device=device)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.acc)
+
+
+def step_stats(times_ms):
+    t = np.asarray(times_ms, dtype=np.float64)
+    return {"median": float(np.median(t)), "mean": float(t.mean()), "min": float(t.min()),
+            "max": float(t.max()), "p10": float(np.percentile(t, 10)), "p90": float(np.percentile(t, 90)),
+            "n": int(t.size)}
+
+
+def timed_launches(fn, steps, stream, flush):
+    """``steps`` launches of ``fn``, each after an L2 flush, each bracketed by
+    CUDA events on ``stream``; returns the per-launch times in ms."""
     import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
 
-    import softmax_l1_norm_gb300 as smla
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
 
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    stream = torch.cuda.current_stream(device)
+def roofline_block(flops, compulsory_bytes, seconds, hbm_gbs, bf16_tf, src, traffic=None):
+    """The binding bound: the larger of the tensor time and the time to move
+    the compulsory bytes at the measured HBM bandwidth."""
+    t_tc = flops / (bf16_tf * 1e12)
+    t_hbm = compulsory_bytes / (hbm_gbs * 1e9)
+    if t_tc >= t_hbm:
+        bound, achieved, peak, unit = "tensor", flops / seconds / 1e12, bf16_tf, "TFLOP/s"
+    else:
+        bound, achieved, peak, unit = "hbm", compulsory_bytes / seconds / 1e9, hbm_gbs, "GB/s"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": traffic, "peak_source": f"{src} (MEASURED_PEAKS.json: bf16 burst, HBM copy)",
+            "roofline_ms": 1000 * max(t_tc, t_hbm), "kernel_ms": 1000 * seconds,
+            "tensor_ms": 1000 * t_tc, "compulsory_hbm_ms": 1000 * t_hbm,
+            "compulsory_bytes": int(compulsory_bytes)}
 
-    w = W.make_config(args.config, seq_len=args.seq_len)
-    name = w.name
-    pairs, flops, bytes_ = workload_numbers(w)
-    alg_bytes = sum(bytes_.values())
 
+def north_star_block(alg_bytes, seconds, hbm_gbs, t_tc_s):
+    """The roofline the work was specified against: every gathered key row
+    counted as HBM traffic.  The keys of these workloads fit in L2, so this
+    bound does not bind; kept for reference only."""
+    t_hbm = alg_bytes / (hbm_gbs * 1e9)
+    return {"bytes_counted": int(alg_bytes), "hbm_ms": 1000 * t_hbm, "tensor_ms": 1000 * t_tc_s,
+            "roofline_ms": 1000 * max(t_hbm, t_tc_s), "kernel_ms": 1000 * seconds,
+            "frac_of_this_bound": 1000 * max(t_hbm, t_tc_s) / (1000 * seconds),
+            "note": "counts every gathered key row as DRAM traffic; the keys are L2-resident, "
+                    "so a fraction above 1 here does not mean skipped work"}
+
+
+def device_inputs(w, device):
+    import torch
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
     host = {
         "q": torch.from_numpy(w.q_bits.view(np.int16)).view(tdt),
@@ -337,28 +424,86 @@ def run_ours(args, world, rank, local):
         "topk_length": None if w.topk_length is None else torch.from_numpy(w.topk_length),
     }
     dev = {k: (None if v is None else v.to(device)) for k, v in host.items()}
-    plan = smla.Plan(layout=w.layout, dtype=w.dtype, num_heads_q=w.G, batch_size=w.batch,
+    return host, dev
+
+
+def make_plan(smla, w):
+    return smla.Plan(layout=w.layout, dtype=w.dtype, num_heads_q=w.G, batch_size=w.batch,
                      max_seqlen_q=w.max_seqlen_q if w.layout == "BSND" else 0,
                      max_seqlen_k=w.k_bits.shape[1] if w.layout == "BSND" else w.max_seqlen_k,
                      topk=w.topk, mask_mode=w.mask_mode, softmax_scale=w.softmax_scale,
                      has_topk_length=w.topk_length is not None,
                      cu_seqlens_q=None if w.cu_seqlens_q is None else w.cu_seqlens_q.tolist(),
                      cu_seqlens_k=None if w.cu_seqlens_k is None else w.cu_seqlens_k.tolist())
+
+
+def other_config_line(smla, n, steps, device, stream, flush):
+    """One configuration other than the headline, timed the same way (after
+    the headline's timed region): median ms per launch and the roofline."""
+    import torch
+    w = W.make_config(n)
+    pairs, flops, bytes_, compulsory = workload_numbers(w)
+    _, dev = device_inputs(w, device)
+    plan = make_plan(smla, w)
     out = torch.empty(plan.output_shape, dtype=torch.float32, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def fn():
+        plan.run(dev["q"], dev["k"], dev["lse"], sparse_indices=dev["indices"],
+                 topk_length=dev["topk_length"], out=out, stream=stream)
+
+    for _ in range(3):
+        flush()
+        fn()
+    times = timed_launches(fn, steps, stream, flush)
+    code, flags = plan.status(stream)
+    if code != smla.SMLA_OK:
+        raise RuntimeError(f"config {n}: device status {code} flags {flags}")
+    st = step_stats(times)
+    hbm_gbs, bf16_tf, src = load_peaks()
+    sec = st["median"] / 1000.0
+    line = {"workload": w.name, "ms_per_launch": st, "pairs_per_s": pairs / sec, "tflops": flops / sec / 1e12,
+            "pairs": pairs, "flops": flops, "roofline": roofline_block(flops, sum(compulsory.values()), sec,
+                                                                      hbm_gbs, bf16_tf, src),
+            "north_star_roofline": north_star_block(sum(bytes_.values()), sec, hbm_gbs,
+                                                    flops / (bf16_tf * 1e12)),
+            "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "num_items", "stages",
+                                                                            "mma_n", "rows_per_item")}}
+    del plan, dev, out
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import softmax_l1_norm_gb300 as smla
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+
+    w = W.make_config(args.config, seq_len=args.seq_len)
+    name = w.name
+    pairs, flops, bytes_, compulsory = workload_numbers(w)
+    alg_bytes = sum(bytes_.values())
+    comp_bytes = sum(compulsory.values())
+
+    host, dev = device_inputs(w, device)
+    plan = make_plan(smla, w)
+    out = torch.empty(plan.output_shape, dtype=torch.float32, device=device)
+    flush = L2Flush(device)
 
     def step():
         plan.run(dev["q"], dev["k"], dev["lse"], sparse_indices=dev["indices"],
                  topk_length=dev["topk_length"], out=out, stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize(device)
     code, flags = plan.status(stream)
     if code != smla.SMLA_OK:
         raise RuntimeError(f"device status {code} flags {flags} during warm-up")
-    # sanity: every output finite and kept slots non-negative
     if not bool(torch.isfinite(out).all()):
         raise RuntimeError("non-finite output")
 
@@ -377,7 +522,7 @@ def run_ours(args, world, rank, local):
         time.sleep(0.3)
         wall0 = time.perf_counter()
         for i in range(args.steps):
-            flush.zero_()          # L2 flush between timed launches (outside the events)
+            flush()                # outside the events
             starts[i].record(stream)
             step()
             ends[i].record(stream)
@@ -391,6 +536,7 @@ def run_ours(args, world, rank, local):
     code, flags = plan.status(stream)
     if code != smla.SMLA_OK:
         raise RuntimeError(f"device status {code} flags {flags} in the timed region")
+    stats = step_stats(times_ms)
 
     # ------------------------------------------------ back-to-back launches (warm L2), secondary
     warm = None
@@ -435,6 +581,8 @@ def run_ours(args, world, rank, local):
                "d2h_bytes_per_step": int(sizes.out_bytes), "steps": e_steps,
                "ms_per_step": 1000 * e2e_s / e_steps}
 
+    hbm_gbs, bf16_tf, src = load_peaks()
+
     # ------------------------------------------------ the forward-LSE modes (outside the timed region)
     lse_modes = None
     if not args.no_lse_modes:
@@ -446,31 +594,31 @@ def run_ours(args, world, rank, local):
                                                                  **extra), 2),
         }
         lse_modes = {}
-        _, bf16_peak, peak_src = load_peaks()
         for mname, (fn, passes) in modes.items():
             for _ in range(3):
-                flush.zero_()
+                flush()
                 fn()
             torch.cuda.synchronize(device)
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.lse_steps)]
-            for a, b in ev:
-                flush.zero_()
-                a.record(stream)
-                fn()
-                b.record(stream)
-            torch.cuda.synchronize(device)
+            ms_list = timed_launches(fn, args.lse_steps, stream, flush)
             code, flags = plan.status(stream)
             if code != smla.SMLA_OK:
                 raise RuntimeError(f"device status {code} flags {flags} in mode {mname}")
-            ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
-            ms = all_max(ms, world, device)
+            st = step_stats(ms_list)
+            ms = all_max(st["median"], world, device)
             tf = passes * flops / (ms / 1000.0) / 1e12
-            lse_modes[mname] = {"ms_per_launch": ms, "launches": args.lse_steps,
-                                "pairs_per_s": world * pairs / (ms / 1000.0), "tflops": tf,
+            lse_modes[mname] = {"ms_per_launch": st, "pairs_per_s": world * pairs / (ms / 1000.0), "tflops": tf,
                                 "mma_passes": passes,
-                                "roofline_tensor": {"achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
-                                                    "frac": tf / bf16_peak, "peak_source": peak_src}}
+                                "roofline_tensor": {"achieved": tf, "peak": bf16_tf, "unit": "TFLOP/s",
+                                                    "frac": tf / bf16_tf, "peak_source": src}}
+
+    # ------------------------------------------------ the other configurations (outside the timed region)
+    others = None
+    if world == 1 and not args.no_other_configs and args.seq_len is None:
+        del host
+        others = {}
+        for n in (1, 2, 3, 4, 5):
+            if n != args.config:
+                others[str(n)] = other_config_line(smla, n, args.other_steps, device, stream, flush)
 
     if rank != 0:
         return 0
@@ -484,39 +632,37 @@ def run_ours(args, world, rank, local):
         cpu = {"value": c_pairs / c_secs, "unit": UNIT, "cores": threads, "kind": "oracle", "cpu": cpu_model(),
                "sample": f"{n_rows} random rows of {name} in {c_secs:.1f}s (fp64 numpy, BLAS threads={threads})"}
 
-    hbm_gbs, bf16_tf, src = load_peaks()
     per_launch_s = kernel_s / args.steps
-    achieved_gbs = alg_bytes / per_launch_s / 1e9
-    achieved_tf = flops / per_launch_s / 1e12
     traffic = profiled_traffic(name)
-    t_hbm = alg_bytes / (hbm_gbs * 1e9)
     t_tc = flops / (bf16_tf * 1e12)
     line = {
         "metric": METRIC, "value": world * pairs * args.steps / max_s, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * max_s / args.steps,
+        "step_ms": stats,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic (seeded numpy; q,k ~ N(0,1); LSE = expected value, see DESIGN)",
+        "dtype": w.dtype,
+        "data": "synthetic (seeded numpy; q,k ~ N(0,1) rounded to the dtype; LSE = its expected value "
+                "ln(kept slots) + scale^2 |q_g|^2 / 2, which leaves the work unchanged)",
         "config": {"workload": name, "layout": w.layout, "B": w.batch, "S1": w.max_seqlen_q,
                    "S2": int(w.k_bits.shape[1]) if w.layout == "BSND" else None, "N1": w.G, "D": w.head_dim,
                    "topk": w.topk, "mask_mode": w.mask_mode, "pairs_per_step": pairs,
                    "flops_per_step": flops, "algorithmic_bytes_per_step": alg_bytes,
-                   "parallelism": f"replicas x{world}", "l2": "flushed (512 MB write) before every timed launch"},
+                   "compulsory_bytes_per_step": comp_bytes,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every timed launch: 512 MB written, then 256 MB read (write-backs "
+                         "of the flush land before the launch)"},
         "tflops": world * flops * args.steps / max_s / 1e12,
-        "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
-                     "achieved": achieved_gbs if t_hbm >= t_tc else achieved_tf,
-                     "peak": hbm_gbs if t_hbm >= t_tc else bf16_tf,
-                     "unit": "GB/s" if t_hbm >= t_tc else "TFLOP/s",
-                     "frac": (achieved_gbs / hbm_gbs) if t_hbm >= t_tc else (achieved_tf / bf16_tf),
-                     "traffic": traffic, "peak_source": src,
-                     "roofline_ms": 1000 * max(t_hbm, t_tc), "kernel_ms": 1000 * per_launch_s},
-        "roofline_tensor": {"achieved": achieved_tf, "peak": bf16_tf, "unit": "TFLOP/s",
-                            "frac": achieved_tf / bf16_tf, "peak_source": src},
+        "roofline": roofline_block(flops, comp_bytes, per_launch_s, hbm_gbs, bf16_tf, src, traffic),
+        "roofline_tensor": {"achieved": flops / per_launch_s / 1e12, "peak": bf16_tf, "unit": "TFLOP/s",
+                            "frac": flops / per_launch_s / 1e12 / bf16_tf, "peak_source": src},
+        "north_star_roofline": north_star_block(alg_bytes, per_launch_s, hbm_gbs, t_tc),
         "clocks": clk,
         "gpu_launches": args.steps,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "lse_modes": lse_modes,
         "warm_back_to_back": warm,
+        "other_configs": others,
         "wall_s_timed_region": wall,
         "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "stages", "mma_n",
                                                                         "smem_bytes", "max_cta_cost",
@@ -545,6 +691,9 @@ def main():
                     help="skip timing the forward-LSE and fused LSE+L1-norm launches")
     ap.add_argument("--lse-steps", type=int, default=50)
     ap.add_argument("--no-warm", action="store_true", help="skip the back-to-back (warm L2) timing")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip timing the other four configurations after the headline")
+    ap.add_argument("--other-steps", type=int, default=20, help="timed launches per other configuration")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="configs 3 and 5 only: a shorter S1 = S2 of the same workload (small profiling case)")
     args = ap.parse_args()

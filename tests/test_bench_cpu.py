@@ -83,7 +83,27 @@ def test_workload_numbers_config3():
     sys.path.insert(0, ROOT)
     import bench
     import workloads as W
-    pairs, flops, b = bench.workload_numbers(W.make_config(3))
+    w = W.make_config(3)
+    pairs, flops, b, comp = bench.workload_numbers(w)
     assert pairs == 805_437_440 and flops == 2 * 512 * pairs
     assert b["k_gathered"] == 6_292_480 * 1024 and b["q"] == 4096 * 128 * 1024
     assert abs(sum(b.values()) - 7.0496e9) < 1e6
+    # compulsory: each tensor once; key j is visible to rows >= j only, so a
+    # few of the last keys are never picked
+    assert "k_gathered" not in comp and 4000 * 1024 <= comp["k_unique"] <= 4096 * 1024
+    assert abs(sum(comp.values()) - 0.6104e9) < 2e6
+    # the binding bound is the tensor one: 824.8 GFLOP at the measured peak
+    # takes longer than moving the compulsory bytes
+    r = bench.roofline_block(flops, sum(comp.values()), 0.7e-3, 6791.4, 1869.3, "measured")
+    assert r["bound"] == "tensor" and abs(r["frac"] - flops / 0.7e-3 / 1e12 / 1869.3) < 1e-12
+    assert r["frac"] < 1.0
+
+
+def test_workload_numbers_dense_unique_keys():
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    w = W.make_config(2)
+    pairs, flops, b, comp = bench.workload_numbers(w)
+    assert pairs == 2 * (512 * 513 // 2) * 16
+    assert comp["k_unique"] == 2 * 512 * 1024 and comp["out"] == 2 * 512 * 512 * 4
