@@ -142,6 +142,9 @@ typedef struct {
   int32_t host_chunks;     /* token chunks smla_l1norm_run_from_host pipelines
                               (copies of one chunk overlap the kernel of the
                               previous one); 0 = one copy, one kernel, one copy */
+  int32_t mma_issuers;     /* threads issuing the L1-norm launch's MMAs: 4 when
+                              the sparse form's N is at most 64 (each owns a
+                              quarter of the head dimension), else 2          */
 } smla_plan_info;
 
 /*
@@ -152,6 +155,15 @@ typedef struct {
  * gives a valid plan whose run() returns at once, as the article's
  * constraints section specifies for an empty q tensor.
  * Synchronous (the work list is uploaded with a blocking copy).
+ *
+ * Every device-side wait of the plan's launches is bounded: 2 s by default,
+ * SMLA_WAIT_TIMEOUT_MS (milliseconds, > 0) as read from the environment here.
+ * A wait that runs out stops the launch's CTA cleanly (copies and MMAs in
+ * flight are drained, tensor memory is released) and sets the timeout flag
+ * that smla_l1norm_get_status() reports; the output is then incomplete.
+ * Test hook: with SMLA_DEBUG_WITHHOLD_Q=1 in the environment at plan
+ * creation, every CTA of the plan's launches skips the load of the first q
+ * chunk of its first work item, so a wait runs out on purpose.
  */
 smla_status smla_l1norm_plan_create(const smla_l1norm_desc *desc, smla_plan **plan_out);
 
@@ -380,7 +392,7 @@ smla_status smla_debug_gather(const smla_plan *plan, int32_t mode, int64_t token
  * the call returns once the copy has taken the host bytes, and the device
  * copy is ordered after earlier work on ``stream``.  The launch shape (CTAs,
  * key-ring depth, shared memory), the validation and the device-side wait
- * limit (SMLA_WAIT_TIMEOUT_NS / SMLA_WAIT_TIMEOUT_MS) are the plan path's;
+ * limit (SMLA_WAIT_TIMEOUT_MS) are the plan path's;
  * smla_debug_noalloc_config() reports the shape without a GPU.
  *
  * Set-up: the first call on each device (with that device current) looks up

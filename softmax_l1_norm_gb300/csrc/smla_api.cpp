@@ -247,6 +247,7 @@ void fill_info(const Geometry& g, const Schedule& s, int num_ctas, int stages, i
   info->mean_cta_cost = s.mean_cost;
   info->q_rows_total = g.q_rows;
   info->k_rows_total = g.k_rows;
+  info->mma_issuers = smla::l1_issuers(g);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -314,11 +315,6 @@ bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int box_ro
 }
 
 int64_t wait_timeout_ns() {
-  if (const char* e = std::getenv("SMLA_WAIT_TIMEOUT_NS")) {
-    char* end = nullptr;
-    const long long ns = std::strtoll(e, &end, 10);
-    if (end != e && ns >= 0) return ns;
-  }
   if (const char* e = std::getenv("SMLA_WAIT_TIMEOUT_MS")) {
     const long long ms = std::atoll(e);
     if (ms > 0) return ms * 1000000LL;
@@ -342,6 +338,7 @@ struct smla_plan {
   WorkItem* d_items = nullptr;
   smla_plan_info info{};
   int64_t timeout_ns = 0;
+  int32_t withhold_q = 0;            // test hook (SMLA_DEBUG_WITHHOLD_Q)
   std::vector<WorkItem> items_host;  // the work list as uploaded, for the gather test hook
   // run_from_host pipeline: token chunks, each with its own work schedule,
   // so that the copies of one chunk overlap the kernel of the previous one
@@ -402,6 +399,7 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   plan->geo = g;
   plan->idesc = smla::make_idesc(desc->dtype, g.n_mma);
   plan->timeout_ns = smla::wait_timeout_ns();
+  if (const char* e = std::getenv("SMLA_DEBUG_WITHHOLD_Q")) plan->withhold_q = std::atoi(e) != 0 ? 1 : 0;
 
   cudaError_t e = cudaGetDevice(&plan->device);
   if (e != cudaSuccess) {
@@ -490,6 +488,7 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
     release_plan(plan);
     return cuda_fail(e, "plan upload");
   }
+  if (plan->info.mma_issuers == 4 && !smla::four_issuers_available()) plan->info.mma_issuers = 2;
   auto* b = static_cast<uint8_t*>(plan->dbuf);
   plan->d_status = reinterpret_cast<int32_t*>(b);
   plan->d_cta_begin = reinterpret_cast<int32_t*>(b + off_begin);
@@ -612,7 +611,9 @@ smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, flo
   p.c_log2 = static_cast<float>(static_cast<double>(plan->desc.softmax_scale) * 1.4426950408889634);
   p.inv_g = 1.0f / static_cast<float>(g.G);
   p.timeout_ns = plan->timeout_ns;
-  cudaError_t e = smla::launch_fused(p, tq, g.sparse, mode, plan->num_ctas, plan->smem,
+  p.withhold_q = plan->withhold_q;
+  const int issuers = mode == smla::kModeL1 ? smla::l1_issuers(g) : 2;
+  cudaError_t e = smla::launch_fused(p, tq, g.sparse, mode, issuers, plan->num_ctas, plan->smem,
                                      reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return SMLA_OK;

@@ -77,6 +77,7 @@ struct KernelParams {
   float c_log2;               // softmax_scale * log2(e)
   float inv_g;                // 1 / G
   int64_t timeout_ns;         // bound on every device-side wait
+  int32_t withhold_q;         // test hook: never load q chunk 0 of each CTA's first item
 };
 
 // Shared-memory footprint for a given MMA N and ring depth.
@@ -95,14 +96,18 @@ enum Mode : int {
   kModeFused = 2,  // the forward LSE, then the L1 norm from it, per work item
 };
 
-// Launch the fused kernel (defined in smla_kernel.cu).
-cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int mode, int grid,
-                         int smem_bytes, cudaStream_t stream);
+// Launch the fused kernel (defined in smla_kernel.cu) with 2 MMA issuers,
+// or 4 (the L1-norm launch of the sparse form with N <= 64 only).
+cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int mode, int issuers,
+                         int grid, int smem_bytes, cudaStream_t stream);
 // Raise every instantiation's dynamic shared-memory cap to the current
 // device's opt-in maximum, once per device (smla_kernel.cu).  The cap only
 // ever rises, so a plan built for a small footprint never lowers it under
 // another plan's larger one.
 cudaError_t configure_fused_for_device();
+// After configure_fused_for_device(): whether the four-issuer L1-norm block
+// (17 warps) fits one SM of the current device.
+bool four_issuers_available();
 // Test hook: the key producers of a launch mode (kModeL1 or kModeLse) alone
 // over work items [it0, it1), each ring stage copied to ``dump`` as the MMA
 // would read it (smla_kernel.cu).  One CTA.
@@ -137,13 +142,17 @@ int visible_keys(int64_t r, int64_t Sq, int64_t Sk, int mask_mode);
 // stages, at least kMinStages (the barrier phases rely on it when several
 // producer groups fill the ring).
 int stages_for(int n_mma, int smem_limit);
+// MMA issuers of the L1-norm launch: four when the accumulator of each is at
+// most 64 columns wide (sparse form, N <= 64), else two.  The ring depth rule
+// is unchanged: with two producer groups filling their stages in order, an
+// even depth keeps every barrier within one phase for two or four issuers.
+inline int l1_issuers(const Shape& s) { return (s.sparse && s.n_mma <= kAccCols / 4) ? 4 : 2; }
 // tcgen05 instruction descriptor, kind::f16, M = 128, N = n_mma.
 uint32_t make_idesc(int dtype, int n_mma);
 // 2-D (rows x 512) SWIZZLE_128B tensor map of a half-precision tensor, boxes
 // of 64 columns x box_rows rows.
 bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int box_rows, int dtype);
-// Bound on every device-side wait: SMLA_WAIT_TIMEOUT_NS (nanoseconds, 0
-// allowed) or SMLA_WAIT_TIMEOUT_MS, else 2 s.
+// Bound on every device-side wait: SMLA_WAIT_TIMEOUT_MS if set (> 0), else 2 s.
 int64_t wait_timeout_ns();
 
 }  // namespace smla

@@ -128,7 +128,8 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
 
 // Wait for the phase with the given parity to complete, for at most
 // ctl.timeout_ns, or until another role has given up.  Returns false on
-// either.
+// either.  (mbarrier.try_wait may suspend the thread until the phase
+// completes, so only a wait that is really stuck reaches the clock check.)
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   return wait_slow(bar, parity, ctl.abort, ctl.status, ctl.timeout_ns);
@@ -243,6 +244,15 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&a)[16], uint32_t (&b)[16
                  "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]));
 }
 
+// Registers written by a tcgen05.ld that an earlier tmem_ld_wait covered:
+// ties them to a point after that wait so that no use moves above it.
+__device__ __forceinline__ void tmem_regs_after_wait(uint32_t (&a)[16]) {
+  asm volatile(""
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
+                 "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]),
+                 "+r"(a[14]), "+r"(a[15]));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -299,8 +309,20 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Warps are spread over the four SM sub-partitions (warp % 4) so that the
 // single MMA-issuing thread shares its sub-partition with as little else as
 // possible: its issue rate is bound by its own instruction latency.
-constexpr int kMmaWarpA = 0;        // even head-dim chunks; sub-partition 0
-constexpr int kMmaWarpB = 2;        // odd head-dim chunks; sub-partition 2
+constexpr int kMmaWarpA = 0;        // issuer 0; sub-partition 0; also allocates TMEM
+// MMA issuers.  Two issuers split each tile's head-dim chunks (even / odd),
+// each accumulating into its own 128-column half of the tile's TMEM buffer.
+// When the MMA N is at most 64, four issuers fit: issuer H takes the chunks
+// c with c % 4 == H, each into its own 64-column quarter, one issuer on each
+// sub-partition (warps 0, 2, 13, 15).
+template <int kIss>
+__device__ __forceinline__ int issuer_index(int warp) {
+  if (warp == 0) return 0;
+  if (warp == 2) return 1;
+  if (kIss == 4 && warp == 13) return 2;
+  if (kIss == 4 && warp == 15) return 3;
+  return -1;
+}
 constexpr int kQWarp = 8;           // sleeps in barrier waits most of the time
 // Producer groups.  A lane's cp.async.mbarrier.arrive.noinc holds the warp
 // until every copy the lane issued before it has landed, so a warp keeps
@@ -328,14 +350,15 @@ __host__ __device__ constexpr int keys_per_lane() {  // 4 key rows per warp inst
 }
 static_assert(kTileKeys % 16 == 0 && kNumChunks % 4 == 0, "groups own the same chunks of every tile");
 static_assert(kMinStages >= 4 && kMinStages % 2 == 0, "ring depth rule");
-template <int kMode>
+template <int kMode, int kIss = 2>
 __host__ __device__ constexpr int kernel_threads() {
-  return kMode == kModeL1 ? 512 : kThreads;
+  return kMode == kModeL1 ? (kIss == 4 ? 544 : 512) : kThreads;
 }
 constexpr int kEpiWarp0 = 4;        // warps 4-7: one warpgroup
 // Producer warp number: warps 1, 3, 9, 11 (sub-partitions 1 and 3), then,
-// for a second group, 13, 15, 10, 14.
-template <int kMode>
+// for a second group, 13, 15, 10, 14 (with four issuers, which take warps 13
+// and 15: 10, 14, 12, 16 of a 17-warp block).
+template <int kMode, int kIss = 2>
 __device__ __forceinline__ int producer_index(int warp) {
   constexpr int n = producer_groups<kMode>() * group_warps<kMode>();
   int i;
@@ -344,10 +367,12 @@ __device__ __forceinline__ int producer_index(int warp) {
     case 3: i = 1; break;
     case 9: i = 2; break;
     case 11: i = 3; break;
-    case 13: i = 4; break;
-    case 15: i = 5; break;
-    case 10: i = 6; break;
-    case 14: i = 7; break;
+    case 13: i = kIss == 4 ? 8 : 4; break;
+    case 15: i = kIss == 4 ? 8 : 5; break;
+    case 10: i = kIss == 4 ? 4 : 6; break;
+    case 14: i = kIss == 4 ? 5 : 7; break;
+    case 12: i = kIss == 4 ? 6 : 8; break;
+    case 16: i = kIss == 4 ? 7 : 8; break;
     default: i = 8;
   }
   return i < n ? i : -1;
@@ -441,7 +466,7 @@ struct MmaCtx {
 // so that a thread owns one head and reduces over the keys.  Both operands
 // are 128-byte-swizzled K-major tiles, so the swap only exchanges the start
 // addresses and the instruction descriptor.
-template <bool kSparse, int kMode, int H>
+template <bool kSparse, int kMode, int kIss, int H>
 __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m, const WaitCtl& ctl) {
   const uint64_t a0 = sdesc_k_major_sw128(m.sK);
   const uint64_t b0 = sdesc_k_major_sw128(m.sQ);
@@ -451,7 +476,7 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
   const uint32_t b_step = static_cast<uint32_t>(m.q_chunk_bytes) >> 4;
   const uint32_t S = static_cast<uint32_t>(p.stages);
   // Ring slot and phase of this issuer's next stage: stage n (8 per tile,
-  // tile-major) uses slot n % S, and this issuer takes every other stage.
+  // tile-major) uses slot n % S, and this issuer takes every kIss-th stage.
   uint32_t kst = H, kph = 0, qit = 0, acc = 0;
   bool ok = true;
   // The barrier test for this issuer's next stage is issued before the
@@ -478,14 +503,14 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
         if (!ok) break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = m.tmem_base + buf * kAccCols + H * kHalfCols;
+      const uint32_t d_tmem = m.tmem_base + buf * kAccCols + H * (kAccCols / kIss);
       const bool last = (t == ntot - 1);
       const bool lse_pass = kMode != kModeL1 && t < nt;
       const uint32_t idesc = static_cast<uint32_t>(lse_pass ? p.idesc_lse : p.idesc);
 #pragma unroll
-      for (int c = H; c < kNumChunks; c += 2) {
+      for (int c = H; c < kNumChunks; c += kIss) {
         const uint32_t sl = kst, ph = kph;
-        kst += 2;
+        kst += kIss;
         if (kst >= S) {
           kst -= S;
           kph ^= 1u;
@@ -500,7 +525,7 @@ __device__ __forceinline__ void mma_issue(const KernelParams& p, const MmaCtx& m
           if (!ok) break;
         }
         const bool ready_next = mbar_test_wait(m.bar_k_full + 8 * kst, kph);
-        if (c + 2 >= kNumChunks)
+        if (c + kIss >= kNumChunks)
           acc_ready = mbar_test_wait(m.bar_acc_empty + 8 * (buf ^ 1u), (((acc + 1) / kAccBufs) & 1u) ^ 1u);
         // the producers' cp.async writes (generic proxy), acquired through
         // the barrier, become visible to the tensor cores (async proxy)
@@ -611,10 +636,8 @@ __device__ __forceinline__ void produce_keys(const KernelParams& p, int pw, int 
 
 }  // namespace
 
-template <bool kSparse, int kMode>
-__global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
-    smla_fused_kernel(const __grid_constant__ KernelParams p,
-                      const __grid_constant__ CUtensorMap tmap_q) {
+template <bool kSparse, int kMode, int kIss>
+__device__ __forceinline__ void fused_body(const KernelParams& p, const CUtensorMap& tmap_q) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -653,10 +676,10 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
       mbar_init(bar_k_empty + 8 * s, 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
-      mbar_init(bar_acc_full + 8 * b, 2);   // one commit per MMA issuer
+      mbar_init(bar_acc_full + 8 * b, kIss);   // one commit per MMA issuer
       mbar_init(bar_acc_empty + 8 * b, 128);
     }
-    mbar_init(bar_teardown, 2);
+    mbar_init(bar_teardown, kIss);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -684,7 +707,8 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
   const int it0 = p.cta_begin[blockIdx.x];
   const int it1 = p.cta_begin[blockIdx.x + 1];
 
-  const int pw = producer_index<kMode>(warp);
+  const int pw = producer_index<kMode, kIss>(warp);
+  const int iss = issuer_index<kIss>(warp);
   if (pw >= 0) {
     // ============================================================ key producers
     produce_keys<kSparse, kMode>(p, pw, lane, sK, bar_k_full, bar_k_empty, ctl, it0, it1);
@@ -706,6 +730,9 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
         for (int c = 0; c < kNumChunks; ++c) {
           ok = wait_bounded(bar_q_empty + 8 * c, (qit & 1u) ^ 1u, ctl);
           if (!ok) break;
+          // test hook: chunk 0 of the first item never arrives, so the MMA
+          // issuers' wait for it runs out and the launch takes its abort path
+          if (p.withhold_q != 0 && qit == 0 && c == 0) continue;
           mbar_arrive_expect_tx(bar_q_full + 8 * c, q_tx);
           tma_load_2d(sQ + c * q_chunk_bytes, &tmap_q, c * kChunkElems, w.q_tok * p.G, bar_q_full + 8 * c);
           q_armed |= 1u << c;
@@ -720,15 +747,19 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarpA || warp == kMmaWarpB) {
+  } else if (iss >= 0) {
     // ============================================================ MMA issuers
     if (lane == 0) {
       const MmaCtx m{sK, sQ, q_chunk_bytes, bar_q_full, bar_q_empty, bar_k_full, bar_k_empty,
                      bar_acc_full, bar_acc_empty, tmem_base, it0, it1};
-      if (warp == kMmaWarpA)
-        mma_issue<kSparse, kMode, 0>(p, m, ctl);
-      else
-        mma_issue<kSparse, kMode, 1>(p, m, ctl);
+      if (iss == 0)
+        mma_issue<kSparse, kMode, kIss, 0>(p, m, ctl);
+      else if (iss == 1)
+        mma_issue<kSparse, kMode, kIss, 1>(p, m, ctl);
+      else if (kIss == 4 && iss == 2)
+        mma_issue<kSparse, kMode, kIss, (kIss == 4 ? 2 : 0)>(p, m, ctl);
+      else if (kIss == 4)
+        mma_issue<kSparse, kMode, kIss, (kIss == 4 ? 3 : 0)>(p, m, ctl);
       // All MMAs this thread issued must be complete before TMEM is released.
       umma_commit(bar_teardown);
       wait_drain(bar_teardown, 0, 200000000);
@@ -932,25 +963,65 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
             }
           };
           const int n = p.n_mma;  // a multiple of 16
-          uint32_t fa[16], ga[16], fb[16], gb[16];
-          tmem_ld16_issue(taddr, fa);
-          tmem_ld16_issue(taddr + kHalfCols, ga);
-          tmem_ld_wait(fa, ga);
-          for (int c0 = 0; c0 < n; c0 += 32) {
-            const bool has_b = c0 + 16 < n;
-            const bool has_a = c0 + 32 < n;
-            if (has_b) {
-              tmem_ld16_issue(taddr + c0 + 16, fb);
-              tmem_ld16_issue(taddr + kHalfCols + c0 + 16, gb);
+          if constexpr (kIss == 4) {
+            // Four partial sums of 64 columns (N <= 64), added as
+            // (q0 + q1) + (q2 + q3) per 16-column group.  Two loads are in
+            // flight at a time (the 17-warp block has 96 registers a
+            // thread): parts 0 and 1 of the next group load while this
+            // group's exponentials run.
+            constexpr int kQ = kAccCols / 4;
+            uint32_t qa[16], qb[16];
+            uint64_t xx[8];
+            tmem_ld16_issue(taddr, qa);
+            tmem_ld16_issue(taddr + kQ, qb);
+#pragma unroll 1
+            for (int c0 = 0; c0 < n; c0 += 16) {
+              tmem_ld_wait(qa, qb);
+#pragma unroll
+              for (int k = 0; k < 16; k += 2)
+                xx[k / 2] = add_f32x2(pack_f32x2(__uint_as_float(qa[k]), __uint_as_float(qa[k + 1])),
+                                      pack_f32x2(__uint_as_float(qb[k]), __uint_as_float(qb[k + 1])));
+              tmem_ld16_issue(taddr + 2 * kQ + c0, qa);
+              tmem_ld16_issue(taddr + 3 * kQ + c0, qb);
+              tmem_ld_wait(qa, qb);
+#pragma unroll
+              for (int k = 0; k < 16; k += 2)
+                xx[k / 2] = add_f32x2(xx[k / 2], add_f32x2(pack_f32x2(__uint_as_float(qa[k]), __uint_as_float(qa[k + 1])),
+                                                           pack_f32x2(__uint_as_float(qb[k]), __uint_as_float(qb[k + 1]))));
+              if (c0 + 16 < n) {
+                tmem_ld16_issue(taddr + c0 + 16, qa);
+                tmem_ld16_issue(taddr + kQ + c0 + 16, qb);
+              }
+              const float2* nl2 = reinterpret_cast<const float2*>(NL + c0);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float2 nl = nl2[k];
+                float y0, y1;
+                unpack_f32x2(fma_f32x2(xx[k], c2c2, pack_f32x2(nl.x, nl.y)), y0, y1);
+                s01 = add_f32x2(s01, pack_f32x2(fast_exp2(y0), fast_exp2(y1)));
+              }
             }
-            l1_16(fa, ga, c0);
-            if (has_b) tmem_ld_wait(fb, gb);
-            if (has_a) {
-              tmem_ld16_issue(taddr + c0 + 32, fa);
-              tmem_ld16_issue(taddr + kHalfCols + c0 + 32, ga);
+          } else {
+            uint32_t fa[16], ga[16], fb[16], gb[16];
+            tmem_ld16_issue(taddr, fa);
+            tmem_ld16_issue(taddr + kHalfCols, ga);
+            tmem_ld_wait(fa, ga);
+            for (int c0 = 0; c0 < n; c0 += 32) {
+              const bool has_b = c0 + 16 < n;
+              const bool has_a = c0 + 32 < n;
+              if (has_b) {
+                tmem_ld16_issue(taddr + c0 + 16, fb);
+                tmem_ld16_issue(taddr + kHalfCols + c0 + 16, gb);
+              }
+              l1_16(fa, ga, c0);
+              if (has_b) tmem_ld_wait(fb, gb);
+              if (has_a) {
+                tmem_ld16_issue(taddr + c0 + 32, fa);
+                tmem_ld16_issue(taddr + kHalfCols + c0 + 32, ga);
+              }
+              if (has_b) l1_16(fb, gb, c0 + 16);
+              if (has_a) tmem_ld_wait(fa, ga);
             }
-            if (has_b) l1_16(fb, gb, c0 + 16);
-            if (has_a) tmem_ld_wait(fa, ga);
           }
           tc_fence_before();
           mbar_arrive(bar_acc_empty + 8 * buf);
@@ -959,23 +1030,51 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
             p.out[static_cast<int64_t>(w.q_tok) * p.topk + slot] = valid ? (s0 + s1) * p.inv_g : 0.f;
         } else {
           // Dense form: columns r*G + g belong to token q_tok + r; 16
-          // columns at a time, the next 16 loading meanwhile.
+          // columns at a time, the next 16 loading meanwhile.  The 16
+          // exponentials of a chunk are computed independently first (column
+          // pairs in packed f32x2), then summed into the running token sum:
+          // with G a multiple of 16 a chunk lies inside one token and is
+          // summed as a tree; otherwise column by column, closing a token
+          // every G columns.  Token boundaries are the same for every thread.
           const int j = slot;
           float s = 0.f;
           int g_in = 0, r = 0;
+          const bool whole_chunks = (p.G & 15) == 0;
+          auto store_token = [&]() {
+            if (r < w.nrows && j < p.width) {
+              const bool v = (j < e.Sk) && (w.r0 + r < e.Sq) &&
+                             (p.mask_mode == 0 || j <= w.r0 + r + e.Sk - e.Sq);
+              p.out[static_cast<int64_t>(w.q_tok + r) * p.width + j] = v ? s * p.inv_g : 0.f;
+            }
+            s = 0.f;
+            g_in = 0;
+            ++r;
+          };
           auto dense16 = [&](const uint32_t (&fa)[16], const uint32_t (&ga)[16], int c0) {
+            float e16[16];
+            const float2* nl2 = reinterpret_cast<const float2*>(NL + c0);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              s += fast_exp2(fmaf(__uint_as_float(fa[k]) + __uint_as_float(ga[k]), c2, NL[c0 + k]));
-              if (++g_in == p.G) {
-                if (r < w.nrows && j < p.width) {
-                  const bool v = (j < e.Sk) && (w.r0 + r < e.Sq) &&
-                                 (p.mask_mode == 0 || j <= w.r0 + r + e.Sk - e.Sq);
-                  p.out[static_cast<int64_t>(w.q_tok + r) * p.width + j] = v ? s * p.inv_g : 0.f;
-                }
-                s = 0.f;
-                g_in = 0;
-                ++r;
+            for (int k = 0; k < 16; k += 2) {
+              const float2 nl = nl2[k / 2];
+              const uint64_t x = add_f32x2(pack_f32x2(__uint_as_float(fa[k]), __uint_as_float(fa[k + 1])),
+                                           pack_f32x2(__uint_as_float(ga[k]), __uint_as_float(ga[k + 1])));
+              float y0, y1;
+              unpack_f32x2(fma_f32x2(x, c2c2, pack_f32x2(nl.x, nl.y)), y0, y1);
+              e16[k] = fast_exp2(y0);
+              e16[k + 1] = fast_exp2(y1);
+            }
+            if (whole_chunks) {
+              float t8[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) t8[k] = e16[2 * k] + e16[2 * k + 1];
+              s += ((t8[0] + t8[1]) + (t8[2] + t8[3])) + ((t8[4] + t8[5]) + (t8[6] + t8[7]));
+              g_in += 16;
+              if (g_in == p.G) store_token();
+            } else {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                s += e16[k];
+                if (++g_in == p.G) store_token();
               }
             }
           };
@@ -1027,6 +1126,21 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
                  "r"(kAccBufs * kAccCols)
                  : "memory");
   }
+}
+
+template <bool kSparse, int kMode, int kIss>
+__global__ void __launch_bounds__(kernel_threads<kMode, kIss>(), 1)
+    smla_fused_kernel(const __grid_constant__ KernelParams p, const __grid_constant__ CUtensorMap tmap_q) {
+  fused_body<kSparse, kMode, kIss>(p, tmap_q);
+}
+
+// The L1-norm launch with four MMA issuers runs 17 warps.  Warps are dealt
+// to the four sub-partitions in turn, and each sub-partition has a quarter
+// of the register file: five warps on one of them leave 96 registers a
+// thread.  The host still checks with the occupancy API that one block fits.
+__global__ void __launch_bounds__(kernel_threads<kModeL1, 4>(), 1)
+    smla_fused_kernel_l1_4iss(const __grid_constant__ KernelParams p, const __grid_constant__ CUtensorMap tmap_q) {
+  fused_body<true, kModeL1, 4>(p, tmap_q);
 }
 
 // A bounded wait on a barrier that nothing completes: checks that the
@@ -1082,7 +1196,7 @@ __global__ void __launch_bounds__(kernel_threads<kMode>(), 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  const int pw = producer_index<kMode>(warp);
+  const int pw = producer_index<kMode, 2>(warp);
   if (pw >= 0) {
     produce_keys<kSparse, kMode>(p, pw, lane, sK, bar_k_full, bar_k_empty, ctl, it0, it1);
   } else if (warp == 0) {
@@ -1133,10 +1247,14 @@ cudaError_t launch_gather_dump(const KernelParams& p, bool sparse, int mode, int
   return cudaGetLastError();
 }
 
+namespace {
+constexpr int kMaxDevices = 64;
+bool four_issuers_fit[kMaxDevices] = {};
+}  // namespace
+
 cudaError_t configure_fused_for_device() {
   // Once per device, every instantiation's cap goes to the opt-in maximum;
   // a launch still asks for exactly the shared memory its plan needs.
-  constexpr int kMaxDevices = 64;
   static std::mutex mu;
   static bool done[kMaxDevices] = {};
   int dev = 0, optin = 0;
@@ -1148,12 +1266,13 @@ cudaError_t configure_fused_for_device() {
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   const void* fns[] = {
-      reinterpret_cast<const void*>(smla_fused_kernel<true, kModeL1>),
-      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeL1>),
-      reinterpret_cast<const void*>(smla_fused_kernel<true, kModeLse>),
-      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeLse>),
-      reinterpret_cast<const void*>(smla_fused_kernel<true, kModeFused>),
-      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeFused>),
+      reinterpret_cast<const void*>(smla_fused_kernel<true, kModeL1, 2>),
+      reinterpret_cast<const void*>(smla_fused_kernel_l1_4iss),
+      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeL1, 2>),
+      reinterpret_cast<const void*>(smla_fused_kernel<true, kModeLse, 2>),
+      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeLse, 2>),
+      reinterpret_cast<const void*>(smla_fused_kernel<true, kModeFused, 2>),
+      reinterpret_cast<const void*>(smla_fused_kernel<false, kModeFused, 2>),
       reinterpret_cast<const void*>(smla_gather_dump_kernel<true, kModeL1>),
       reinterpret_cast<const void*>(smla_gather_dump_kernel<false, kModeL1>),
       reinterpret_cast<const void*>(smla_gather_dump_kernel<true, kModeLse>),
@@ -1162,21 +1281,44 @@ cudaError_t configure_fused_for_device() {
     e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e != cudaSuccess) return e;
   }
+  int blocks = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, smla_fused_kernel_l1_4iss, kernel_threads<kModeL1, 4>(),
+                                                    optin);
+  if (e != cudaSuccess) return e;
+  four_issuers_fit[dev] = blocks >= 1;
   done[dev] = true;
   return cudaSuccess;
 }
 
-cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int mode, int grid,
-                         int smem_bytes, cudaStream_t stream) {
+bool four_issuers_available() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  return four_issuers_fit[dev];
+}
+
+cudaError_t launch_fused(const KernelParams& p, const CUtensorMap& tmap_q, bool sparse, int mode, int issuers,
+                         int grid, int smem_bytes, cudaStream_t stream) {
   const dim3 g(grid);
-  const dim3 b1(kernel_threads<kModeL1>()), b(kThreads);
+  const dim3 b1(kernel_threads<kModeL1, 2>()), b14(kernel_threads<kModeL1, 4>()), b(kThreads);
+  if (issuers == 4) {  // the L1-norm launch, sparse form, N <= 64
+    if (mode != kModeL1 || !sparse || p.n_mma > kAccCols / 4) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices && four_issuers_fit[dev]) {
+      smla_fused_kernel_l1_4iss<<<g, b14, smem_bytes, stream>>>(p, tmap_q);
+      return cudaGetLastError();
+    }
+    issuers = 2;  // the 17-warp block does not fit this device: two issuers
+  }
+  if (issuers != 2) return cudaErrorInvalidValue;
   switch (mode * 2 + (sparse ? 1 : 0)) {
-    case kModeL1 * 2 + 1: smla_fused_kernel<true, kModeL1><<<g, b1, smem_bytes, stream>>>(p, tmap_q); break;
-    case kModeL1 * 2: smla_fused_kernel<false, kModeL1><<<g, b1, smem_bytes, stream>>>(p, tmap_q); break;
-    case kModeLse * 2 + 1: smla_fused_kernel<true, kModeLse><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
-    case kModeLse * 2: smla_fused_kernel<false, kModeLse><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
-    case kModeFused * 2 + 1: smla_fused_kernel<true, kModeFused><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
-    case kModeFused * 2: smla_fused_kernel<false, kModeFused><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeL1 * 2 + 1: smla_fused_kernel<true, kModeL1, 2><<<g, b1, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeL1 * 2: smla_fused_kernel<false, kModeL1, 2><<<g, b1, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeLse * 2 + 1: smla_fused_kernel<true, kModeLse, 2><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeLse * 2: smla_fused_kernel<false, kModeLse, 2><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeFused * 2 + 1: smla_fused_kernel<true, kModeFused, 2><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
+    case kModeFused * 2: smla_fused_kernel<false, kModeFused, 2><<<g, b, smem_bytes, stream>>>(p, tmap_q); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -127,6 +127,7 @@ extern "C" smla_status smla_debug_noalloc_config(const smla_l1norm_desc* desc, i
   info->out_width = s.width;
   info->q_rows_total = s.q_rows;
   info->k_rows_total = s.k_rows;
+  info->mma_issuers = smla::l1_issuers(s);
   return SMLA_OK;
 }
 
@@ -216,7 +217,8 @@ extern "C" smla_status smla_l1norm_run_noalloc(const smla_l1norm_desc* desc, con
   p.inv_g = 1.0f / static_cast<float>(s.G);
   p.timeout_ns = smla::wait_timeout_ns();
   e = smla::configure_fused_for_device();
-  if (e == cudaSuccess) e = smla::launch_fused(p, tq, s.sparse, smla::kModeL1, ls.ctas, ls.smem, cstream);
+  if (e == cudaSuccess)
+    e = smla::launch_fused(p, tq, s.sparse, smla::kModeL1, smla::l1_issuers(s), ls.ctas, ls.smem, cstream);
   if (e != cudaSuccess) return SMLA_ERR_CUDA;
   return SMLA_OK;
 }

@@ -142,6 +142,22 @@ def test_key_ring_depth_is_even_for_every_head_count(topk):
         assert info.smem_bytes <= 232448
 
 
+def test_mma_issuers_follow_the_accumulator_width():
+    """The sparse L1-norm launch uses four MMA issuers when each one's
+    accumulator (the MMA N, G padded to 16) fits in a quarter of a 256-column
+    TMEM buffer; the dense form and wider sparse N use two."""
+    for G in (1, 16, 48, 64, 65, 80, 128):
+        _, _, info = smla.schedule_host(152, want_items=False, num_heads_q=G, batch_size=1, max_seqlen_q=8,
+                                        max_seqlen_k=512, topk=256, mask_mode=0, softmax_scale=0.05)
+        assert info.mma_issuers == (4 if info.mma_n <= 64 else 2), (G, info.mma_n, info.mma_issuers)
+        nf = smla.noalloc_config(152, 232448, num_heads_q=G, batch_size=1, max_seqlen_q=8,
+                                 max_seqlen_k=512, topk=256, mask_mode=0, softmax_scale=0.05)
+        assert nf.mma_issuers == info.mma_issuers
+    _, _, info = smla.schedule_host(152, want_items=False, num_heads_q=16, batch_size=1, max_seqlen_q=64,
+                                    max_seqlen_k=512, topk=0, mask_mode=3, softmax_scale=0.05)
+    assert info.mma_issuers == 2
+
+
 def test_schedule_balance_on_the_causal_topk2048_shape():
     """4096 tokens, G=128, topk 2048 causal: per-token work runs from 1 to 16
     tiles; longest-first assignment keeps the heaviest CTA within a few % of

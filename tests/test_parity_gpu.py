@@ -238,19 +238,21 @@ def test_wait_timeout_probe_reports_and_returns(lib):
 
 
 def test_fused_kernel_waits_give_up_and_report(lib, monkeypatch):
-    """A plan made with a device wait limit of 0 ns: the first wait of the
-    fused kernel that is not already satisfied gives up, sets the CTA's abort
-    flag and the timeout bit; every role leaves its loop, copies and MMAs in
-    flight are drained and TMEM is released.  Each launch mode reports
-    SMLA_ERR_TIMEOUT, and afterwards the context still computes the oracle's
-    result with a normal plan."""
+    """A plan whose launches never load one q chunk (a test hook) and whose
+    device waits are bounded by 30 ms: the MMA issuers' wait for that chunk
+    runs out, sets the CTA's abort flag and the timeout bit; every role leaves
+    its loop, copies and MMAs in flight are drained and TMEM is released.
+    Each launch mode reports SMLA_ERR_TIMEOUT, and afterwards the context
+    still computes the oracle's result with a normal plan."""
     w = W.make_workload(layout="BSND", dtype="bf16", B=1, S1=64, S2=2500, G=128, topk=2048, mask_mode=3,
                         seed=5200, lse=None)
     exact_lse(oracle, w)
     t = to_device(w)
-    monkeypatch.setenv("SMLA_WAIT_TIMEOUT_NS", "0")
+    monkeypatch.setenv("SMLA_WAIT_TIMEOUT_MS", "30")
+    monkeypatch.setenv("SMLA_DEBUG_WITHHOLD_Q", "1")
     plan0 = lib.Plan(**plan_kwargs(w))
-    monkeypatch.delenv("SMLA_WAIT_TIMEOUT_NS")
+    monkeypatch.delenv("SMLA_WAIT_TIMEOUT_MS")
+    monkeypatch.delenv("SMLA_DEBUG_WITHHOLD_Q")
     runs = {
         "l1": lambda: plan0.run(t["q"], t["k"], t["lse"], sparse_indices=t["idx"], topk_length=t["tl"]),
         "lse": lambda: plan0.softmax_lse(t["q"], t["k"], sparse_indices=t["idx"], topk_length=t["tl"]),

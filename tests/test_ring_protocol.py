@@ -29,8 +29,9 @@ import random
 import pytest
 
 
-def simulate(S, groups, tiles, seed, stall_prob=0.08):
-    """Run the ring protocol once; return (violations, stages consumed)."""
+def simulate(S, groups, tiles, seed, stall_prob=0.08, issuers=2):
+    """Run the ring protocol once; return (violations, stages consumed).
+    Issuer h takes the stages n with n % issuers == h."""
     rng = random.Random(seed)
     N = 8 * tiles
     full = [0] * S    # completed phases of each slot's full barrier
@@ -53,13 +54,13 @@ def simulate(S, groups, tiles, seed, stall_prob=0.08):
         return (count & 1) != parity
 
     prod_next = {g: g for g in range(groups)}      # next stage of each producer group
-    iss_next = {h: h for h in range(2)}            # next stage of each issuer
-    iss_ready = {h: False for h in range(2)}       # next stage already acquired by a test
+    iss_next = {h: h for h in range(issuers)}      # next stage of each issuer
+    iss_ready = {h: False for h in range(issuers)}  # next stage already acquired by a test
     pipe_free = [0.0]
     consumed = [0]
     for g in range(groups):
         push(0.0, "prod", g)
-    for h in range(2):
+    for h in range(issuers):
         push(0.0, "iss", h)
 
     steps = 0
@@ -95,7 +96,7 @@ def simulate(S, groups, tiles, seed, stall_prob=0.08):
                 if full[s] != u + 1:
                     violations.append(("issuer wait", n, full[s], u + 1))
             # test the next own stage before issuing this one's MMAs
-            m = n + 2
+            m = n + issuers
             iss_ready[who] = False
             if m < N:
                 sm, um = m % S, m // S
@@ -106,8 +107,8 @@ def simulate(S, groups, tiles, seed, stall_prob=0.08):
             start = max(t + 40.0, pipe_free[0])
             pipe_free[0] = start + 256.0 * (0.9 + 0.2 * rng.random())
             push(pipe_free[0], "mma_done", n)
-            iss_next[who] = n + 2
-            push(t + delay(400.0), "iss", who)
+            iss_next[who] = n + issuers
+            push(t + delay(400.0 * issuers / 2), "iss", who)
         elif kind == "mma_done":
             empty[who % S] += 1
             consumed[0] += 1
@@ -149,3 +150,36 @@ def test_odd_ring_depth_with_two_groups_can_pass_a_test_early(S):
     assert found, "expected an early pass with an odd ring depth and two groups"
     kind, n, seen, wanted = found[0]
     assert seen == wanted - 2, "the barrier was two phases behind"
+
+
+@pytest.mark.parametrize("S", [4, 6, 8, 10, 12])
+@pytest.mark.parametrize("groups", [1, 2])
+def test_four_issuers_with_one_or_two_groups_and_an_even_depth_are_safe(S, groups):
+    """Four MMA issuers (each owning every fourth stage, as the L1-norm launch
+    runs them when the heads fit in 64 accumulator columns).  An issuer about
+    to take stage m holds stage m - 4; the slot's previous stage m - S has the
+    parity of m - 4 whenever S is even, so with one or two producer groups
+    (each filling its stages in order) it was filled before m - 4: no barrier
+    is ever two phases behind.  The general rule: S = issuers (mod groups)."""
+    for seed in range(20):
+        violations, consumed = simulate(S, groups, tiles=30, seed=11000 + 10 * S + groups + seed,
+                                        stall_prob=0.3, issuers=4)
+        assert violations == [], (S, groups, seed, violations[:3])
+        assert consumed == 240
+
+
+def test_four_issuers_and_four_groups_need_a_depth_multiple_of_four():
+    """With four producer groups as well, six slots break the rule: stage
+    m - 6 belongs to another group and can still be unfilled."""
+    found = []
+    for seed in range(80):
+        violations, _ = simulate(6, 4, tiles=30, seed=12000 + seed, stall_prob=0.3, issuers=4)
+        found += violations
+        if found:
+            break
+    assert found, "expected an early pass with four groups, four issuers and six slots"
+    kind, n, seen, wanted = found[0]
+    assert seen == wanted - 2
+    for seed in range(20):
+        violations, consumed = simulate(8, 4, tiles=30, seed=12500 + seed, stall_prob=0.3, issuers=4)
+        assert violations == [] and consumed == 240

@@ -194,14 +194,14 @@ def test_noalloc_after_plans_of_other_footprints():
         exact_lse(oracle, w)
     want = {id(w): oracle.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **oracle_kwargs(w))
             for w in (big, small, mid)}
-    got_big, plan_big, t_big, st = run_gpu(lib, big)
-    assert st[0] == lib.SMLA_OK
+    got_big, plan_big, t_big, st = run_gpu(smla, big)
+    assert st[0] == smla.SMLA_OK
     assert_close(got_big, want[id(big)], what="G=128 plan")
-    got_small, plan_small, _, st = run_gpu(lib, small)
-    assert st[0] == lib.SMLA_OK and plan_small.info.smem_bytes < plan_big.info.smem_bytes
+    got_small, plan_small, _, st = run_gpu(smla, small)
+    assert st[0] == smla.SMLA_OK and plan_small.info.smem_bytes < plan_big.info.smem_bytes
     assert_close(got_small, want[id(small)], what="G=8 plan")
-    again, _, _, st = run_gpu(lib, big, plan=plan_big, tensors=t_big)
-    assert st[0] == lib.SMLA_OK
+    again, _, _, st = run_gpu(smla, big, plan=plan_big, tensors=t_big)
+    assert st[0] == smla.SMLA_OK
     assert_close(again, want[id(big)], what="G=128 plan after the G=8 plan")
     t = to_device(mid)
     out = torch.full(want[id(mid)].shape, float("nan"), dtype=torch.float32, device="cuda")
