@@ -53,6 +53,20 @@ its reason in the design notes of this repository):
       Sk' = min(Sk, seqused_k[b]); query rows r >= Sq' are all 0, keys
       j >= Sk' are masked, and mask_mode 3 uses the effective lengths
       (j <= r + Sk' - Sq').
+  R12 compressed keys (parameter table: cmp_ratio, the compression rate of k,
+      1..128; cmp_residual_k, per batch entry the remainder of S2 // cmpRatio,
+      required when mask_mode = 3 and cmp_ratio != 1; the TND example passes
+      a K of T2 rows with cmp_ratio 128 and expects an output T2 wide, so K
+      holds the compressed keys).  With ratio c, key j of a sequence stands for
+      the original key positions j*c .. j*c + c - 1 of an original sequence of
+      L = Sk*c + res positions, res = cmp_residual_k[b] (clamped to 0..c-1;
+      0 when not given).  mask_mode 3 applies the right-down causal rule to
+      original positions and keeps key j only when its whole block is
+      visible: j*c + c - 1 <= r + L - Sq (the article leaves the rule for a
+      partly visible block open; this reading never lets a query see a block
+      that holds a later position).  With c = 1 this is reading R6; with
+      mask_mode 0 the ratio does not matter.  Under seqused_k, Sk is the cut
+      key count and L = Sk'*c + res.
 
 Inputs are the rounded half-precision tensors as raw 16-bit patterns plus a
 dtype tag; every product and sum is carried out in float64.
@@ -67,7 +81,7 @@ import numpy as np
 __all__ = [
     "decode_half", "token_geometry", "slot_key_positions", "slot_valid",
     "simple_softmax", "reduce_sum_g_mean", "softmax_l1_norm",
-    "softmax_l1_norm_rows", "softmax_lse",
+    "softmax_l1_norm_rows", "softmax_lse", "original_key_length",
 ]
 
 
@@ -128,20 +142,22 @@ def slot_key_positions(idx_row: Optional[np.ndarray], width: int) -> np.ndarray:
 
 
 def slot_valid(j: np.ndarray, *, r: int, Sq: int, Sk: int, mask_mode: int,
-               topk_len: Optional[int]) -> np.ndarray:
+               topk_len: Optional[int], cmp_ratio: int = 1, orig_len: Optional[int] = None) -> np.ndarray:
     """Which slots contribute (readings R5, R6).
 
     A slot is valid iff its key position lies in the sequence (0 <= j < Sk),
     its slot number is below topk_length when that tensor is given (the
     article: topk_length is the number of keys each query row actually
-    selected), and, for mask_mode 3, j <= r + Sk - Sq.
+    selected), and, for mask_mode 3, j <= r + Sk - Sq -- with compressed keys
+    (R12) the block of key j must end at or before r + L - Sq, L = orig_len.
     """
+    L = Sk if orig_len is None else int(orig_len)
     i = np.arange(len(j))
     ok = (j >= 0) & (j < Sk)
     if topk_len is not None:
         ok &= i < int(topk_len)
     if mask_mode == 3:
-        ok &= j <= (r + Sk - Sq)
+        ok &= (j + 1) * int(cmp_ratio) - 1 <= (r + L - Sq)
     elif mask_mode != 0:
         raise ValueError("mask_mode must be 0 (none) or 3 (rightDownCausal)")
     return ok
@@ -204,8 +220,15 @@ def _effective(geo_t, seqused_q, seqused_k):
     return b, r, Sq, k0, Sk
 
 
+def original_key_length(Sk: int, b: int, cmp_ratio: int, cmp_residual_k) -> int:
+    """L = Sk * c + res of sequence b (reading R12)."""
+    c = int(cmp_ratio)
+    res = 0 if cmp_residual_k is None else int(np.asarray(cmp_residual_k).reshape(-1)[b])
+    return Sk * c + min(max(res, 0), c - 1)
+
+
 def _row_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length, width, mask_mode,
-               seqused_q=None, seqused_k=None):
+               seqused_q=None, seqused_k=None, cmp_ratio=1, cmp_residual_k=None):
     b, r, Sq, k0, Sk = _effective(geo[t], seqused_q, seqused_k)
     idx_row = None
     tl = None
@@ -214,7 +237,11 @@ def _row_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length, width, mask_m
         if topk_length is not None:
             tl = int(np.asarray(topk_length).reshape(-1)[t])
     j = slot_key_positions(idx_row, width)
-    valid = slot_valid(j, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=tl)
+    if int(cmp_ratio) == 1:
+        valid = slot_valid(j, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=tl)
+    else:
+        valid = slot_valid(j, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=tl, cmp_ratio=int(cmp_ratio),
+                           orig_len=original_key_length(Sk, b, cmp_ratio, cmp_residual_k))
     if r >= Sq:                                # a query row that does not take part
         valid = np.zeros_like(valid)
     rows = np.where(valid, k0 + j, 0)          # key rows (any row for invalid slots)
@@ -230,7 +257,7 @@ def softmax_l1_norm_rows(q_bits, k_bits, softmax_lse, rows: Iterable[int], *, dt
                          sparse_indices=None, topk_length=None, cu_seqlens_q=None,
                          cu_seqlens_k=None, softmax_scale: float = 1.0, max_seqlen_k: int = 0,
                          mask_mode: int = 0, layout: str = "BSND", seqused_q=None,
-                         seqused_k=None) -> np.ndarray:
+                         seqused_k=None, cmp_ratio: int = 1, cmp_residual_k=None) -> np.ndarray:
     """The operator for selected query tokens only; returns float32 (len(rows), width).
 
     ``rows`` are token indices (b*S1 + r for BSND, the packed index for TND).
@@ -243,7 +270,7 @@ def softmax_l1_norm_rows(q_bits, k_bits, softmax_lse, rows: Iterable[int], *, dt
     out = np.zeros((len(rows), width), dtype=np.float32)
     for n, t in enumerate(rows):
         q_row, sel_k, valid = _row_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length,
-                                         width, mask_mode, seqused_q, seqused_k)
+                                         width, mask_mode, seqused_q, seqused_k, cmp_ratio, cmp_residual_k)
         p = simple_softmax(q_row, sel_k, valid, lse[t], softmax_scale)      # stage 2
         out[n] = reduce_sum_g_mean(p).astype(np.float32)                    # stage 3 (R10)
     return out
@@ -252,7 +279,8 @@ def softmax_l1_norm_rows(q_bits, k_bits, softmax_lse, rows: Iterable[int], *, dt
 def softmax_l1_norm(q_bits, k_bits, softmax_lse, *, dtype: str, sparse_indices=None,
                     topk_length=None, cu_seqlens_q=None, cu_seqlens_k=None,
                     softmax_scale: float = 1.0, max_seqlen_k: int = 0, mask_mode: int = 0,
-                    layout: str = "BSND", seqused_q=None, seqused_k=None) -> np.ndarray:
+                    layout: str = "BSND", seqused_q=None, seqused_k=None, cmp_ratio: int = 1,
+                    cmp_residual_k=None) -> np.ndarray:
     """The whole operator.  Output float32 (B,S1,1,width) or (T1,1,width)
     ([SMLA] infershape: BSND gives (B, S1, N2, K or S2); TND reading R4)."""
     q_bits = np.asarray(q_bits)
@@ -262,7 +290,7 @@ def softmax_l1_norm(q_bits, k_bits, softmax_lse, *, dtype: str, sparse_indices=N
                                cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k,
                                softmax_scale=softmax_scale, max_seqlen_k=max_seqlen_k,
                                mask_mode=mask_mode, layout=layout, seqused_q=seqused_q,
-                               seqused_k=seqused_k)
+                               seqused_k=seqused_k, cmp_ratio=cmp_ratio, cmp_residual_k=cmp_residual_k)
     if layout == "TND":
         return out.reshape(n_tok, 1, -1)
     return out.reshape(q_bits.shape[0], q_bits.shape[1], 1, -1)
@@ -274,7 +302,8 @@ def softmax_l1_norm(q_bits, k_bits, softmax_lse, *, dtype: str, sparse_indices=N
 def softmax_lse(q_bits, k_bits, *, dtype: str, rows: Optional[Iterable[int]] = None,
                 sparse_indices=None, topk_length=None, cu_seqlens_q=None, cu_seqlens_k=None,
                 softmax_scale: float = 1.0, max_seqlen_k: int = 0, mask_mode: int = 0,
-                layout: str = "BSND", seqused_q=None, seqused_k=None) -> np.ndarray:
+                layout: str = "BSND", seqused_q=None, seqused_k=None, cmp_ratio: int = 1,
+                cmp_residual_k=None) -> np.ndarray:
     """softmaxLse of the forward attention pass over the same valid set:
     lse[t, g] = log sum_{valid i} exp(scale * q[t,g] . k[j_i]), float64,
     -inf for a row with no valid slot.  ([SMLA] 参数说明: softmax_lse is the
@@ -287,7 +316,7 @@ def softmax_lse(q_bits, k_bits, *, dtype: str, rows: Optional[Iterable[int]] = N
     out = np.full((len(rows), G), -math.inf, dtype=np.float64)
     for n, t in enumerate(rows):
         q_row, sel_k, valid = _row_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length,
-                                         width, mask_mode, seqused_q, seqused_k)
+                                         width, mask_mode, seqused_q, seqused_k, cmp_ratio, cmp_residual_k)
         if not valid.any():
             continue
         x = (q_row @ sel_k[valid].T) * float(softmax_scale)

@@ -443,6 +443,118 @@ def pin_seqused_truncation(o):
             assert np.all(np.isneginf(lse_cut[q0 + sq:q0 + Sq])), f"case {ci} seq {b}: unused rows' lse"
 
 
+def _expand_compressed(w, c, res):
+    """The compressed workload ``w`` (TND) restated on original positions:
+    sequence b gets L_b = Sk_b*c + res_b key rows, compressed key j sits at
+    position j*c + c - 1 (the other rows are zero and never selected), and
+    every index j in [0, Sk_b) becomes j*c + c - 1 (-1 stays -1; indices past
+    the sequence stay past it).  Returns (k_bits, sparse_indices, cu_seqlens_k)."""
+    seqs = list(w.sequences())
+    kv = w.k_bits.reshape(-1, D)
+    rows, cu = [], [0]
+    for b, q0, Sq, k0, Sk in seqs:
+        L = Sk * c + int(res[b])
+        kb = np.zeros((L, D), np.uint16)
+        if Sk:
+            kb[np.arange(Sk) * c + c - 1] = kv[k0:k0 + Sk]
+        rows.append(kb)
+        cu.append(cu[-1] + L)
+    k_exp = np.concatenate(rows).reshape(-1, 1, D) if rows else np.zeros((0, 1, D), np.uint16)
+    if w.sparse_indices is not None:
+        idx = w.sparse_indices.reshape(w.n_tokens, -1).astype(np.int64)
+        tab = w.token_table()
+        Sk_t = tab[:, 4:5]
+        L_t = np.array([Sk * c + int(res[b]) for (b, _, _, _, Sk) in seqs])[tab[:, 0]][:, None]
+        inside = (idx >= 0) & (idx < Sk_t)
+        idx_exp = np.where(inside, idx * c + c - 1, np.where(idx < 0, idx, L_t + idx))
+    else:
+        width = w.out_width
+        idx_exp = np.tile(np.arange(width) * c + c - 1, (w.n_tokens, 1))
+        tab = w.token_table()
+        idx_exp = np.where(np.arange(width)[None, :] < tab[:, 4:5], idx_exp, -1)
+    return k_exp, idx_exp.astype(np.int32).reshape(w.n_tokens, 1, -1), np.array(cu, np.int32)
+
+
+def pin_compressed_keys(o):
+    """Compressed keys (reading R12: key j covers original positions j*c ..
+    j*c + c - 1 of L = Sk*c + cmp_residual_k positions; mask 3 keeps a key
+    when its whole block is visible)."""
+    g = _golden()
+    qb, kb = _hand_dense(2, 3, [0.0, 1.0, 2.0])
+    for res, name in ((0, "compressed_dense_r4_res0"), (1, "compressed_dense_r4_res1")):
+        case = g[name]
+        cr = np.array([res], np.int32)
+        lse = o.softmax_lse(qb, kb, dtype="bf16", softmax_scale=1.0, mask_mode=3, cmp_ratio=4, cmp_residual_k=cr)
+        _close(lse[:, 0], [_ev(x) for x in case["lse"]], rtol=1e-12, what=f"{name} lse")
+        out = o.softmax_l1_norm(qb, kb, lse.astype(np.float32).reshape(1, 1, 2, 1), dtype="bf16",
+                                softmax_scale=1.0, mask_mode=3, cmp_ratio=4, cmp_residual_k=cr)
+        _close(out.reshape(2, 3), [[_ev(x) for x in r] for r in case["out"]], what=f"{name} out")
+    qb12, _ = _hand_dense(12, 3, [0.0, 1.0, 2.0])
+    lse = o.softmax_lse(qb12, kb, dtype="bf16", softmax_scale=1.0, mask_mode=3, cmp_ratio=4,
+                        cmp_residual_k=np.array([0], np.int32))
+    out = o.softmax_l1_norm(qb12, kb, np.where(np.isneginf(lse), 0, lse).astype(np.float32).reshape(1, 1, 12, 1),
+                            dtype="bf16", softmax_scale=1.0, mask_mode=3, cmp_ratio=4,
+                            cmp_residual_k=np.array([0], np.int32)).reshape(12, 3)
+    assert list((out != 0).sum(axis=1)) == g["compressed_dense_r4_s1_12"]["visible"]
+    assert np.all(np.isneginf(lse[:3, 0])) and np.all(np.isfinite(lse[3:, 0]))
+
+    # ratio 1 (residual 0) is the operator without compression; with mask 0
+    # neither the ratio nor the residual matters
+    for w in tiny_cases():
+        with_exact_lse(o, w)
+        base = o.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **kw(w))
+        zeros = np.zeros(w.batch, np.int32)
+        assert np.array_equal(base, o.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, cmp_ratio=1,
+                                                      cmp_residual_k=zeros, **kw(w)))
+        if w.mask_mode == 0:
+            other = o.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, cmp_ratio=16,
+                                      cmp_residual_k=np.full(w.batch, 7, np.int32), **kw(w))
+            assert np.array_equal(base, other), "mask 0 must not depend on the compression"
+
+    # the compressed operator equals the uncompressed one on the original
+    # positions, with each compressed key at the end of its block
+    cases = [
+        dict(layout="TND", dtype="bf16", seqlens_q=[5, 9, 3], seqlens_k=[7, 4, 6], G=3, topk=5, mask_mode=3,
+             seed=800, c=4, res=[1, 3, 0]),
+        dict(layout="TND", dtype="fp16", seqlens_q=[6, 2], seqlens_k=[5, 9], G=2, topk=0, mask_mode=3,
+             seed=801, c=3, res=[2, 0], max_seqlen_k=10),
+        dict(layout="TND", dtype="bf16", seqlens_q=[40], seqlens_k=[3], G=2, topk=0, mask_mode=3,
+             seed=802, c=16, res=[5]),
+    ]
+    for case in cases:
+        c, res = case.pop("c"), np.array(case.pop("res"), np.int32)
+        w = W.make_workload(lse=None, **case)
+        rng = np.random.Generator(np.random.PCG64(case["seed"]))
+        W.set_lse_rows(w, rng.uniform(0.5, 3.0, size=(w.n_tokens, w.G)).astype(np.float32))
+        if w.sparse_indices is not None:
+            w.sparse_indices = rng.integers(-2, max(w.k_bits.shape[0], 2) + 1,
+                                            size=w.sparse_indices.shape).astype(np.int32)
+        got = o.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, cmp_ratio=c, cmp_residual_k=res, **kw(w))
+        lse_c = o.softmax_lse(w.q_bits, w.k_bits, cmp_ratio=c, cmp_residual_k=res, **kw(w))
+        k_exp, idx_exp, cu_k = _expand_compressed(w, c, res)
+        sub = dict(dtype=w.dtype, softmax_scale=w.softmax_scale, mask_mode=w.mask_mode, layout="TND",
+                   cu_seqlens_q=w.cu_seqlens_q, cu_seqlens_k=cu_k, sparse_indices=idx_exp,
+                   topk_length=w.topk_length, max_seqlen_k=int(np.diff(cu_k).max()))
+        want = o.softmax_l1_norm(w.q_bits, k_exp, w.softmax_lse, **sub).reshape(w.n_tokens, -1)
+        assert np.array_equal(got.reshape(w.n_tokens, -1), want[:, :got.reshape(w.n_tokens, -1).shape[1]]), \
+            f"compressed case {case['seed']} differs from its expansion"
+        assert np.array_equal(lse_c, o.softmax_lse(w.q_bits, k_exp, **sub)), f"lse of case {case['seed']}"
+
+    # the article's TND call: 16 queries, 2048 compressed keys of ratio 128,
+    # residual 0, right-down causal, dense: output (T1, 1, 2048); query r
+    # keeps floor((r + 2048*128 - 16 + 1) / 128) keys (row 0 misses the last
+    # block, which holds later positions; row 15 keeps all 2048)
+    w = W.make_workload(layout="TND", dtype="fp16", seqlens_q=[16], seqlens_k=[2048], G=2, topk=0, mask_mode=3,
+                        seed=803, lse=None)
+    kwc = dict(kw(w), cmp_ratio=128, cmp_residual_k=np.zeros(1, np.int32))
+    lse = o.softmax_lse(w.q_bits, w.k_bits, **kwc)
+    out = o.softmax_l1_norm(w.q_bits, w.k_bits, lse.astype(np.float32).reshape(1, 16, 2), **kwc)
+    assert out.shape == (16, 1, 2048) and np.all(np.isfinite(out))
+    kept = (out.reshape(16, 2048) != 0).sum(axis=1)
+    assert list(kept) == [min(2048, (r + 2048 * 128 - 16 + 1) // 128) for r in range(16)]
+    assert kept[0] == 2047 and kept[15] == 2048
+
+
 ALL_PINS = [pin_hand_sparse, pin_hand_causal, pin_row_sums, pin_g1_textbook_softmax,
             pin_brute_force, pin_sparse_equals_dense, pin_layout_equivalence,
-            pin_head_symmetries, pin_seqused_truncation, pin_lse_logsumexp]
+            pin_head_symmetries, pin_seqused_truncation, pin_lse_logsumexp, pin_compressed_keys]

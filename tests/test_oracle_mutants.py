@@ -44,8 +44,8 @@ def _mut_divide_by_slots(m):
 
 def _mut_causal_off_by_one(m):
     orig = m.slot_valid
-    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
-        ok = orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=0, topk_len=topk_len)
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len, **extra):
+        ok = orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=0, topk_len=topk_len, **extra)
         if mask_mode == 3:
             ok &= j < (r + Sk - Sq)
         return ok
@@ -54,8 +54,8 @@ def _mut_causal_off_by_one(m):
 
 def _mut_causal_top_left(m):
     orig = m.slot_valid
-    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
-        ok = orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=0, topk_len=topk_len)
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len, **extra):
+        ok = orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=0, topk_len=topk_len, **extra)
         if mask_mode == 3:
             ok &= j <= r
         return ok
@@ -64,15 +64,15 @@ def _mut_causal_top_left(m):
 
 def _mut_ignore_topk_length(m):
     orig = m.slot_valid
-    m.slot_valid = lambda j, *, r, Sq, Sk, mask_mode, topk_len: orig(
+    m.slot_valid = lambda j, *, r, Sq, Sk, mask_mode, topk_len, **extra: orig(
         j, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=None)
 
 
 def _mut_mask_on_slot(m):
     """causal test applied to the slot number instead of the key position"""
     orig = m.slot_valid
-    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
-        ok = orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=0, topk_len=topk_len)
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len, **extra):
+        ok = orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=0, topk_len=topk_len, **extra)
         if mask_mode == 3:
             ok &= np.arange(len(j)) <= (r + Sk - Sq)
         return ok
@@ -93,7 +93,7 @@ def _mut_tnd_key_offset(m):
 
 def _mut_keep_out_of_range(m):
     orig = m.slot_valid
-    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len, **extra):
         ok = orig(np.where(j >= Sk, 0, j), r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=topk_len)
         return ok
     m.slot_valid = f
@@ -125,8 +125,8 @@ def _mut_seqused_q_ignored(m):
 def _mut_seqused_causal_full_lengths(m):
     """seqused applied to the masks but the causal offset kept on full lengths"""
     orig_valid = m.slot_valid
-    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
-        return orig_valid(j, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=topk_len)
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len, **extra):
+        return orig_valid(j, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=topk_len, **extra)
     m.slot_valid = f
     orig_eff = m._effective
     def eff(g, sq, sk):
@@ -171,15 +171,15 @@ def _mut_bf16_read_as_fp16(m):
 def _mut_minus_one_wraps(m):
     """index -1 taken as the last key of the sequence (negative indexing)"""
     orig = m.slot_valid
-    def f(j, *, r, Sq, Sk, mask_mode, topk_len):
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len, **extra):
         jj = np.where(j < 0, Sk - 1, j)
-        return orig(jj, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=topk_len)
+        return orig(jj, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=topk_len, **extra)
     m.slot_valid = f
     orig_terms = m._row_terms
     def terms(t, geo, qv, kv, dtype, sparse_indices, topk_length, width, mask_mode,
-              seqused_q=None, seqused_k=None):
+              seqused_q=None, seqused_k=None, *rest):
         q_row, sel_k, valid = orig_terms(t, geo, qv, kv, dtype, sparse_indices, topk_length, width,
-                                         mask_mode, seqused_q, seqused_k)
+                                         mask_mode, seqused_q, seqused_k, *rest)
         if sparse_indices is not None:
             b, r, Sq, k0, Sk = m._effective(geo[t], seqused_q, seqused_k)
             idx_row = np.asarray(sparse_indices).reshape(len(geo), -1)[t].astype(np.int64)
@@ -205,13 +205,39 @@ def _mut_slots_in_key_order(m):
     m.slot_key_positions = f
 
 
+def _mut_cmp_block_start(m):
+    """compressed keys kept when their block merely starts at a visible position"""
+    orig = m.slot_valid
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len, cmp_ratio=1, orig_len=None):
+        ok = orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=0, topk_len=topk_len)
+        if mask_mode == 3:
+            L = Sk if orig_len is None else orig_len
+            ok &= j * cmp_ratio <= r + L - Sq
+        return ok
+    m.slot_valid = f
+
+
+def _mut_cmp_residual_ignored(m):
+    """the original key length taken as Sk * cmp_ratio, without the residual"""
+    m.original_key_length = lambda Sk, b, c, res: Sk * int(c)
+
+
+def _mut_cmp_ratio_ignored(m):
+    """compressed keys masked as if each stood for one original position"""
+    orig = m.slot_valid
+    def f(j, *, r, Sq, Sk, mask_mode, topk_len, cmp_ratio=1, orig_len=None):
+        return orig(j, r=r, Sq=Sq, Sk=Sk, mask_mode=mask_mode, topk_len=topk_len)
+    m.slot_valid = f
+
+
 MUTANTS = [_mut_drop_scale, _mut_sign, _mut_sum_not_mean, _mut_divide_by_slots,
            _mut_causal_off_by_one, _mut_causal_top_left, _mut_ignore_topk_length,
            _mut_mask_on_slot, _mut_lse_head_order, _mut_tnd_key_offset,
            _mut_keep_out_of_range, _mut_log2, _mut_lse_no_scale, _mut_seqused_q_ignored,
            _mut_seqused_causal_full_lengths, _mut_lse_base2, _mut_lse_drops_topk_length,
            _mut_lse_mask_off, _mut_bf16_read_as_fp16, _mut_minus_one_wraps,
-           _mut_seqused_k_ignored, _mut_slots_in_key_order]
+           _mut_seqused_k_ignored, _mut_slots_in_key_order, _mut_cmp_block_start,
+           _mut_cmp_residual_ignored, _mut_cmp_ratio_ignored]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=lambda f: f.__name__[5:])
@@ -222,6 +248,8 @@ def test_mutant_is_caught(mutant):
     for pin in P.ALL_PINS:
         try:
             pin(m)
-        except Exception as e:  # AssertionError or a crash both count as caught
+        except (AssertionError, IndexError) as e:
+            # a wrong value, or a gather outside K that the mistake led to;
+            # not a TypeError from a stale override of an oracle function
             failed.append((pin.__name__, type(e).__name__))
     assert failed, f"mutant {mutant.__name__} passed every pin"
