@@ -58,7 +58,8 @@ typedef enum {
   SMLA_ERR_NULLPTR = 1,      /* a required pointer is NULL                         */
   SMLA_ERR_INVALID = 2,      /* a shape / layout / dtype / constraint is violated  */
   SMLA_ERR_UNSUPPORTED = 3,  /* a documented feature this library does not build:
-                                cmp_ratio != 1, mask modes other than 0 and 3     */
+                                mask modes 1 and 2; compressed keys under the
+                                causal mask in smla_l1norm_run_noalloc          */
   SMLA_ERR_CUDA = 4,         /* a CUDA runtime call failed (see get_last_cuda_error) */
   SMLA_ERR_TIMEOUT = 5,      /* a device-side wait gave up (reported by get_status) */
   SMLA_WARN_BAD_INDEX = 6,   /* a sparse index outside [-1, Sk) was seen and treated
@@ -87,7 +88,17 @@ typedef enum { SMLA_MASK_NONE = 0, SMLA_MASK_RIGHT_DOWN_CAUSAL = 3 } smla_mask_m
  *                       topk > 0).
  *   topk                last dimension of sparse_indices; 0 = dense form.
  *   mask_mode           0 (none) or 3 (rightDownCausal).
- *   cmp_ratio           key compression ratio; only 1 is built.
+ *   cmp_ratio           key compression ratio c, 1..128 ([SMLA] 参数说明).  With
+ *                       c > 1, K holds compressed keys: key j of a sequence
+ *                       stands for the original key positions j*c .. j*c+c-1
+ *                       of an original sequence of L = Sk*c + cmp_residual_k
+ *                       positions (Sk = the sequence's rows of K).  Under
+ *                       mask_mode 3 a key is kept only when its whole block
+ *                       is visible: j*c + c - 1 <= r + L - Sq (the article
+ *                       leaves the rule for a partly visible block open; this
+ *                       reading never shows a query a later position).  With
+ *                       mask_mode 0 the ratio changes nothing.  The dense
+ *                       output is as wide as K (compressed positions).
  *   softmax_scale       multiplies q.k before the exp (the article's default
  *                       is 1.0 and it recommends 1/sqrt(head_dim)).
  *   has_topk_length     1 if run() will be given topk_length.
@@ -204,9 +215,9 @@ smla_status smla_l1norm_run(const smla_plan *plan, const void *q, const void *k,
 
 /*
  * The tensors of one call, for smla_l1norm_run_tensors().  Device pointers;
- * the first five and ``out`` as for smla_l1norm_run().  The two optional
- * inputs of the article's parameter table (参数说明) that run() has no slot
- * for:
+ * the first five and ``out`` as for smla_l1norm_run().  The optional inputs
+ * of the article's parameter table (参数说明) that run() has no slot for:
+ * seqused_q, seqused_k (below) and cmp_residual_k (see the field):
  *
  *   seqused_q   (B,) int32 or NULL: query tokens of each sequence that take
  *               part.  Sequence b's query rows r >= min(Sq_b, seqused_q[b])
@@ -230,6 +241,17 @@ typedef struct {
   const int32_t *seqused_q;
   const int32_t *seqused_k;
   float *out;
+  const int32_t *cmp_residual_k; /* (B,) int32: per sequence, the original key
+                                    count minus Sk*cmp_ratio (the remainder of
+                                    the original length // cmp_ratio), read on
+                                    the device and clamped to 0..cmp_ratio-1.
+                                    Required (else SMLA_ERR_NULLPTR) when the
+                                    plan has cmp_ratio != 1 and mask_mode 3;
+                                    ignored otherwise.  run() and
+                                    run_from_host() pass NULL, so such plans
+                                    run through run_tensors() and the LSE
+                                    entry points.  Under seqused_k the original
+                                    length is Sk'*cmp_ratio + cmp_residual_k. */
 } smla_l1norm_tensors;
 
 /* smla_l1norm_run() with every optional input; same errors (NULL ``tensors``

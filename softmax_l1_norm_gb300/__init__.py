@@ -72,7 +72,8 @@ class PlanInfo(ctypes.Structure):
 
 class _Tensors(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("q", "k", "softmax_lse", "sparse_indices", "topk_length", "seqused_q", "seqused_k", "out")]
+                ("q", "k", "softmax_lse", "sparse_indices", "topk_length", "seqused_q", "seqused_k", "out",
+                 "cmp_residual_k")]
 
 
 class IoSizes(ctypes.Structure):
@@ -270,14 +271,14 @@ class Plan:
         return s
 
     def run(self, q, k, softmax_lse, sparse_indices=None, topk_length=None, out=None, stream=None,
-            seqused_q=None, seqused_k=None):
-        """``smla_l1norm_run`` (``smla_l1norm_run_tensors`` when ``seqused_q`` or
-        ``seqused_k`` is given: int32 CUDA tensors of one value per sequence);
-        allocates ``out`` (fp32) if not given."""
+            seqused_q=None, seqused_k=None, cmp_residual_k=None):
+        """``smla_l1norm_run`` (``smla_l1norm_run_tensors`` when ``seqused_q``,
+        ``seqused_k`` or ``cmp_residual_k`` is given: int32 CUDA tensors of one
+        value per sequence); allocates ``out`` (fp32) if not given."""
         if out is None:
             import torch
             out = torch.empty(self.output_shape, dtype=torch.float32, device=q.device)
-        if seqused_q is None and seqused_k is None:
+        if seqused_q is None and seqused_k is None and cmp_residual_k is None:
             code = self._lib.smla_l1norm_run(
                 self._h, _ptr(q, "q"), _ptr(k, "k", required=False), _ptr(softmax_lse, "softmax_lse"),
                 _ptr(sparse_indices, "sparse_indices", required=False),
@@ -288,7 +289,8 @@ class Plan:
                      _ptr(sparse_indices, "sparse_indices", required=False),
                      _ptr(topk_length, "topk_length", required=False),
                      _ptr(seqused_q, "seqused_q", required=False),
-                     _ptr(seqused_k, "seqused_k", required=False), _ptr(out, "out"))
+                     _ptr(seqused_k, "seqused_k", required=False), _ptr(out, "out"),
+                     _ptr(cmp_residual_k, "cmp_residual_k", required=False))
         code = self._lib.smla_l1norm_run_tensors(self._h, ctypes.byref(t), _stream_handle(stream))
         _check(code, "smla_l1norm_run_tensors")
         return out
@@ -302,29 +304,30 @@ class Plan:
             return (1, int(self.info.num_tokens), G)
         return (int(d.get("batch_size", 0)), 1, int(d.get("max_seqlen_q", 0)), G)
 
-    def _tensors(self, q, k, sparse_indices, topk_length, seqused_q, seqused_k, out):
+    def _tensors(self, q, k, sparse_indices, topk_length, seqused_q, seqused_k, out, cmp_residual_k=None):
         return _Tensors(_ptr(q, "q"), _ptr(k, "k", required=False), None,
                         _ptr(sparse_indices, "sparse_indices", required=False),
                         _ptr(topk_length, "topk_length", required=False),
                         _ptr(seqused_q, "seqused_q", required=False),
-                        _ptr(seqused_k, "seqused_k", required=False), _ptr(out, "out", required=False))
+                        _ptr(seqused_k, "seqused_k", required=False), _ptr(out, "out", required=False),
+                        _ptr(cmp_residual_k, "cmp_residual_k", required=False))
 
     def softmax_lse(self, q, k, sparse_indices=None, topk_length=None, lse_out=None, stream=None,
-                    seqused_q=None, seqused_k=None):
+                    seqused_q=None, seqused_k=None, cmp_residual_k=None):
         """``smla_softmax_lse_run``: the forward LSE over the kept slots
         (natural log, fp32, -inf for a row with none); allocates ``lse_out``
         if not given."""
         if lse_out is None:
             import torch
             lse_out = torch.empty(self.lse_shape, dtype=torch.float32, device=q.device)
-        t = self._tensors(q, k, sparse_indices, topk_length, seqused_q, seqused_k, None)
+        t = self._tensors(q, k, sparse_indices, topk_length, seqused_q, seqused_k, None, cmp_residual_k)
         code = self._lib.smla_softmax_lse_run(self._h, ctypes.byref(t), _ptr(lse_out, "lse_out"),
                                               _stream_handle(stream))
         _check(code, "smla_softmax_lse_run")
         return lse_out
 
     def run_fused_lse(self, q, k, sparse_indices=None, topk_length=None, out=None, lse_out=None,
-                      stream=None, seqused_q=None, seqused_k=None):
+                      stream=None, seqused_q=None, seqused_k=None, cmp_residual_k=None):
         """``smla_l1norm_run_fused_lse``: the forward LSE and the operator
         from it in one launch; returns (out, lse_out)."""
         import torch
@@ -332,7 +335,7 @@ class Plan:
             out = torch.empty(self.output_shape, dtype=torch.float32, device=q.device)
         if lse_out is None:
             lse_out = torch.empty(self.lse_shape, dtype=torch.float32, device=q.device)
-        t = self._tensors(q, k, sparse_indices, topk_length, seqused_q, seqused_k, out)
+        t = self._tensors(q, k, sparse_indices, topk_length, seqused_q, seqused_k, out, cmp_residual_k)
         code = self._lib.smla_l1norm_run_fused_lse(self._h, ctypes.byref(t), _ptr(lse_out, "lse_out"),
                                                    _stream_handle(stream))
         _check(code, "smla_l1norm_run_fused_lse")
@@ -414,7 +417,7 @@ _PLAN_CACHE = {}
 
 def sparse_flash_mla_softmax_l1_norm(q, k, softmax_lse, *, sparse_indices=None, cu_seqlens_q=None,
                                      cu_seqlens_k=None, seqused_q=None, seqused_k=None,
-                                     topk_length=None, softmax_scale: float = 1.0,
+                                     cmp_residual_k=None, topk_length=None, softmax_scale: float = 1.0,
                                      max_seqlen_k: int = 0, cmp_ratio: int = 1, mask_mode: int = 0,
                                      layout_q: str = "BSND", layout_k: str = "BSND",
                                      stream=None):
@@ -451,4 +454,4 @@ def sparse_flash_mla_softmax_l1_norm(q, k, softmax_lse, *, sparse_indices=None, 
                     cu_seqlens_q=cq, cu_seqlens_k=ck)
         _PLAN_CACHE[key] = plan
     return plan.run(q, k, softmax_lse, sparse_indices=sparse_indices, topk_length=topk_length, stream=stream,
-                    seqused_q=seqused_q, seqused_k=seqused_k)
+                    seqused_q=seqused_q, seqused_k=seqused_k, cmp_residual_k=cmp_residual_k)

@@ -80,7 +80,6 @@ smla_status check_desc(const smla_l1norm_desc* d, Shape* g) {
   if (d->mask_mode == 1 || d->mask_mode == 2) return SMLA_ERR_UNSUPPORTED;
   if (d->mask_mode != 0 && d->mask_mode != 3) return SMLA_ERR_INVALID;
   if (d->cmp_ratio < 1 || d->cmp_ratio > 128) return SMLA_ERR_INVALID;       // range 1..128
-  if (d->cmp_ratio != 1) return SMLA_ERR_UNSUPPORTED;
   if (d->topk < 0) return SMLA_ERR_INVALID;
   if (!std::isfinite(d->softmax_scale)) return SMLA_ERR_INVALID;
   if (d->has_topk_length != 0 && d->has_topk_length != 1) return SMLA_ERR_INVALID;
@@ -131,9 +130,11 @@ smla_status check_desc(const smla_l1norm_desc* d, Shape* g) {
   return SMLA_OK;
 }
 
-int visible_keys(int64_t r, int64_t Sq, int64_t Sk, int mask_mode) {
+int visible_keys(int64_t r, int64_t Sq, int64_t Sk, int mask_mode, int cmp_ratio) {
   if (mask_mode == 0) return static_cast<int>(Sk);
-  return static_cast<int>(std::min<int64_t>(Sk, std::max<int64_t>(0, r + Sk - Sq + 1)));
+  const int64_t c = std::max(1, cmp_ratio);
+  const int64_t d = r + Sk * c + (c - 1) - Sq + 1;  // the largest residual, c - 1
+  return static_cast<int>(std::min<int64_t>(Sk, std::max<int64_t>(0, d) / c));
 }
 
 }  // namespace smla
@@ -170,7 +171,7 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
         if (d->topk_length_hint != nullptr) {
           n = std::min<int64_t>(std::max<int32_t>(d->topk_length_hint[tok], 0), d->topk);
         } else if (d->has_topk_length) {
-          n = std::min<int64_t>(d->topk, visible_keys(r, Sq, Sk, d->mask_mode));
+          n = std::min<int64_t>(d->topk, visible_keys(r, Sq, Sk, d->mask_mode, d->cmp_ratio));
         } else {
           n = d->topk;
         }
@@ -187,7 +188,7 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
       for (int64_t r0 = 0; r0 < Sq; r0 += g.R) {
         if (g.q0[b] + r0 < tok_lo || g.q0[b] + r0 >= tok_hi) continue;
         const int64_t nrows = std::min<int64_t>(g.R, Sq - r0);
-        const int64_t vis = visible_keys(r0 + nrows - 1, Sq, Sk, d->mask_mode);
+        const int64_t vis = visible_keys(r0 + nrows - 1, Sq, Sk, d->mask_mode, d->cmp_ratio);
         const int64_t tiles = ceil_div(std::min<int64_t>(vis, g.width), smla::kTileKeys);
         WorkItem w{static_cast<int32_t>(g.q0[b] + r0), static_cast<int32_t>(nrows), static_cast<int32_t>(r0),
                    static_cast<int32_t>(g.k0[b]), static_cast<int32_t>(Sq), static_cast<int32_t>(Sk),
@@ -574,9 +575,13 @@ smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, flo
   if (g.k_rows > 0 && t->k == nullptr) return SMLA_ERR_NULLPTR;
   if (g.sparse && t->sparse_indices == nullptr) return SMLA_ERR_NULLPTR;
   if (plan->desc.has_topk_length && t->topk_length == nullptr) return SMLA_ERR_NULLPTR;
+  // compressed keys with the causal mask need the per-sequence residual
+  const bool needs_res = plan->desc.cmp_ratio != 1 && plan->desc.mask_mode == 3;
+  if (needs_res && t->cmp_residual_k == nullptr) return SMLA_ERR_NULLPTR;
   if (!aligned16(t->q) || (t->k != nullptr && !aligned16(t->k))) return SMLA_ERR_INVALID;
   const void* a4[] = {wants_lse_in ? t->softmax_lse : nullptr, wants_out ? t->out : nullptr, lse_out,
-                      t->sparse_indices, t->topk_length, t->seqused_q, t->seqused_k};
+                      t->sparse_indices, t->topk_length, t->seqused_q, t->seqused_k,
+                      needs_res ? t->cmp_residual_k : nullptr};
   for (const void* a : a4)
     if (a != nullptr && !aligned4(a)) return SMLA_ERR_INVALID;
 
@@ -605,6 +610,8 @@ smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, flo
   p.topk = g.sparse ? plan->desc.topk : 0;
   p.width = g.width;
   p.mask_mode = plan->desc.mask_mode;
+  p.cmp_ratio = plan->desc.cmp_ratio;
+  p.cmp_res = needs_res ? t->cmp_residual_k : nullptr;
   p.stages = plan->stages;
   p.idesc = static_cast<int32_t>(plan->idesc);
   p.idesc_lse = static_cast<int32_t>(smla::make_idesc(plan->desc.dtype, smla::kTileKeys));
@@ -640,7 +647,7 @@ smla_status smla_l1norm_run_fused_lse(const smla_plan* plan, const smla_l1norm_t
 smla_status smla_l1norm_run(const smla_plan* plan, const void* q, const void* k, const float* softmax_lse,
                             const int32_t* sparse_indices, const int32_t* topk_length, float* out,
                             smla_stream_t stream) {
-  const smla_l1norm_tensors t{q, k, softmax_lse, sparse_indices, topk_length, nullptr, nullptr, out};
+  const smla_l1norm_tensors t{q, k, softmax_lse, sparse_indices, topk_length, nullptr, nullptr, out, nullptr};
   return smla_l1norm_run_tensors(plan, &t, stream);
 }
 
@@ -687,7 +694,7 @@ smla_status smla_l1norm_run_from_host(const smla_plan* plan, const void* h_q, co
   // stream returns each chunk's output rows as soon as its kernel is done.
   // H2D and D2H use different copy engines, so the only serial part is the
   // host-to-device traffic.  The caller's stream waits for the last copy.
-  const smla_l1norm_tensors t{d_q, d_k, d_lse, d_indices, d_topk_length, nullptr, nullptr, d_out};
+  const smla_l1norm_tensors t{d_q, d_k, d_lse, d_indices, d_topk_length, nullptr, nullptr, d_out, nullptr};
   if (t.q == nullptr || t.softmax_lse == nullptr || t.out == nullptr) return SMLA_ERR_NULLPTR;
   const int64_t n_tok = plan->geo.n_tokens;
   auto per_token = [n_tok](size_t total) { return total / static_cast<size_t>(n_tok); };
@@ -797,6 +804,7 @@ smla_status smla_debug_gather(const smla_plan* plan, int32_t mode, int64_t token
   p.topk = g.sparse ? plan->desc.topk : 0;
   p.width = g.width;
   p.mask_mode = plan->desc.mask_mode;
+  p.cmp_ratio = plan->desc.cmp_ratio;
   p.stages = plan->stages;
   p.timeout_ns = plan->timeout_ns;
   cudaError_t e = smla::configure_fused_for_device();
@@ -812,7 +820,9 @@ const char* smla_status_string(smla_status s) {
     case SMLA_OK: return "SMLA_OK";
     case SMLA_ERR_NULLPTR: return "SMLA_ERR_NULLPTR: a required pointer is NULL";
     case SMLA_ERR_INVALID: return "SMLA_ERR_INVALID: shape, layout, dtype or constraint violated";
-    case SMLA_ERR_UNSUPPORTED: return "SMLA_ERR_UNSUPPORTED: documented feature not built (cmp_ratio != 1, mask modes 1/2)";
+    case SMLA_ERR_UNSUPPORTED:
+      return "SMLA_ERR_UNSUPPORTED: documented feature not built (mask modes 1/2; compressed causal keys in "
+             "smla_l1norm_run_noalloc)";
     case SMLA_ERR_CUDA: return "SMLA_ERR_CUDA: a CUDA call failed";
     case SMLA_ERR_TIMEOUT: return "SMLA_ERR_TIMEOUT: a device-side wait gave up";
     case SMLA_WARN_BAD_INDEX: return "SMLA_WARN_BAD_INDEX: a sparse index outside [-1, Sk) was treated as masked";

@@ -62,6 +62,7 @@ struct KernelParams {
   const int32_t* topk_len;    // (tokens) or null
   const int32_t* seqused_q;   // (batch) participating query rows per sequence, or null
   const int32_t* seqused_k;   // (batch) participating keys per sequence, or null
+  const int32_t* cmp_res;     // (batch) cmp_residual_k, or null (compressed keys, mask 3)
   float* out;                 // (tokens, width); unused by the LSE-only mode
   float* lse_out;             // (tokens, G) forward LSE written by the LSE modes, else null
   int32_t G;                  // heads per key head
@@ -71,6 +72,7 @@ struct KernelParams {
   int32_t topk;               // 0 = dense
   int32_t width;              // output row length
   int32_t mask_mode;          // 0 or 3
+  int32_t cmp_ratio;          // original key positions per key of K (1 = uncompressed)
   int32_t stages;             // key ring depth
   int32_t idesc;              // tcgen05 instruction descriptor: A = keys, B = q (M 128, N n_mma)
   int32_t idesc_lse;          // the same for the LSE pass: A = q rows, B = keys (M 128, N 128)
@@ -137,7 +139,10 @@ struct Shape {
 // description; fills ``s`` on success.  No CUDA call.
 smla_status check_desc(const smla_l1norm_desc* d, Shape* s);
 // Keys of a sequence visible from local row r (mask_mode 3), or all of them.
-int visible_keys(int64_t r, int64_t Sq, int64_t Sk, int mask_mode);
+// With compressed keys (cmp_ratio c > 1) the residual is read on the device;
+// the host takes the largest one (c - 1), an upper bound used for sizing
+// work only.
+int visible_keys(int64_t r, int64_t Sq, int64_t Sk, int mask_mode, int cmp_ratio = 1);
 // Deepest key ring that fits in ``smem_limit`` bytes with an even number of
 // stages, at least kMinStages (the barrier phases rely on it when several
 // producer groups fill the ring).

@@ -393,6 +393,21 @@ __device__ __forceinline__ EffLen effective_lengths(const KernelParams& p, const
   return e;
 }
 
+// Keys visible to local row r under mask_mode 3: key j is kept iff j <
+// causal_limit.  Right-down causal ([SMLA] 约束说明): row r of Sq queries sees
+// key position j <= r + Sk - Sq.  Compressed keys (cmp_ratio c > 1, [SMLA]
+// 参数说明): key j stands for original positions j*c .. j*c + c - 1 of
+// L = Sk*c + cmp_residual_k original positions and is kept when its whole
+// block is visible, j*c + c - 1 <= r + L - Sq.
+__device__ __forceinline__ int causal_limit(const KernelParams& p, const WorkItem& w, const EffLen& e, int r) {
+  if (p.cmp_ratio == 1) return min(e.Sk, max(0, r + e.Sk - e.Sq + 1));
+  const int c = p.cmp_ratio;
+  const int res = p.cmp_res != nullptr ? min(max(__ldg(p.cmp_res + w.b), 0), c - 1) : 0;
+  const int64_t d = static_cast<int64_t>(r) + static_cast<int64_t>(e.Sk) * c + res - e.Sq + 1;
+  if (d <= 0) return 0;
+  return static_cast<int>(min(d / c, static_cast<int64_t>(e.Sk)));
+}
+
 // Key tiles an item needs, and (sparse form) the clamped topk_length.
 template <bool kSparse>
 __device__ __forceinline__ int item_tiles(const KernelParams& p, const WorkItem& w, int& tl) {
@@ -411,7 +426,7 @@ __device__ __forceinline__ int item_tiles(const KernelParams& p, const WorkItem&
   const int rows = min(w.nrows, e.Sq - w.r0);
   if (rows <= 0) return 0;
   int vis = e.Sk;
-  if (p.mask_mode != 0) vis = min(e.Sk, max(0, w.r0 + rows + e.Sk - e.Sq));
+  if (p.mask_mode != 0) vis = causal_limit(p, w, e, w.r0 + rows - 1);
   vis = min(vis, p.width);
   return (vis + kTileKeys - 1) / kTileKeys;
 }
@@ -782,6 +797,8 @@ __device__ __forceinline__ void fused_body(const KernelParams& p, const CUtensor
       int tl;
       const int nt = item_tiles<kSparse>(p, w, tl);
       const EffLen e = effective_lengths(p, w);
+      // sparse form: the slot's key j is kept iff 0 <= j < vlim
+      const int vlim = (!kSparse || p.mask_mode == 0) ? e.Sk : causal_limit(p, w, e, w.r0);
       if (kMode != kModeL1) {
         // ---------------------------------------------------- LSE pass
         // Thread et owns accumulator row et: head et % G of token
@@ -793,7 +810,7 @@ __device__ __forceinline__ void fused_body(const KernelParams& p, const CUtensor
           const int r = et / p.G;
           if (r < min(w.nrows, e.Sq - w.r0)) {
             limit = e.Sk;
-            if (p.mask_mode != 0) limit = min(e.Sk, max(0, w.r0 + r + e.Sk - e.Sq + 1));
+            if (p.mask_mode != 0) limit = causal_limit(p, w, e, w.r0 + r);
             limit = min(limit, p.width);
           }
         }
@@ -808,8 +825,7 @@ __device__ __forceinline__ void fused_body(const KernelParams& p, const CUtensor
             // the slot masks are shared: each warp publishes its 32 slots
             const int slot = t * kTileKeys + et;
             const int j = j_next;
-            const bool valid = (slot < tl) && (j >= 0) && (j < e.Sk) &&
-                               (p.mask_mode == 0 || j <= w.r0 + e.Sk - e.Sq);
+            const bool valid = (slot < tl) && (j >= 0) && (j < vlim);
             const uint32_t bits = __ballot_sync(0xffffffffu, valid);
             if (lane == 0) vmask[mset + quarter] = bits;
             j_next = (slot + kTileKeys < tl) ? __ldg(idx_row + slot + kTileKeys) : -1;
@@ -920,7 +936,7 @@ __device__ __forceinline__ void fused_body(const KernelParams& p, const CUtensor
         if (kSparse) {
           if (slot < tl) {
             const int j = __ldg(p.idx + static_cast<int64_t>(w.q_tok) * p.topk + slot);
-            valid = (j >= 0) && (j < e.Sk) && (p.mask_mode == 0 || j <= w.r0 + e.Sk - e.Sq);
+            valid = (j >= 0) && (j < vlim);
           }
         }
         const uint32_t buf = acc & (kAccBufs - 1);
@@ -1042,8 +1058,8 @@ __device__ __forceinline__ void fused_body(const KernelParams& p, const CUtensor
           const bool whole_chunks = (p.G & 15) == 0;
           auto store_token = [&]() {
             if (r < w.nrows && j < p.width) {
-              const bool v = (j < e.Sk) && (w.r0 + r < e.Sq) &&
-                             (p.mask_mode == 0 || j <= w.r0 + r + e.Sk - e.Sq);
+              const bool v = (w.r0 + r < e.Sq) &&
+                             (j < (p.mask_mode == 0 ? e.Sk : causal_limit(p, w, e, w.r0 + r)));
               p.out[static_cast<int64_t>(w.q_tok + r) * p.width + j] = v ? s * p.inv_g : 0.f;
             }
             s = 0.f;

@@ -90,7 +90,7 @@ void fill_items(const smla_l1norm_desc* d, const smla::Shape& s) {
       const int64_t nrows = std::min<int64_t>(s.R, Sq - r0);
       int64_t tiles = 0;
       if (!s.sparse) {
-        const int64_t vis = smla::visible_keys(r0 + nrows - 1, Sq, Sk, d->mask_mode);
+        const int64_t vis = smla::visible_keys(r0 + nrows - 1, Sq, Sk, d->mask_mode, d->cmp_ratio);
         tiles = (std::min<int64_t>(vis, s.width) + smla::kTileKeys - 1) / smla::kTileKeys;
       }
       g_items_in_order[n++] = WorkItem{static_cast<int32_t>(q0 + r0), static_cast<int32_t>(nrows),
@@ -137,6 +137,9 @@ extern "C" smla_status smla_l1norm_run_noalloc(const smla_l1norm_desc* desc, con
   smla::Shape s;
   smla_status st = smla::check_desc(desc, &s);
   if (st != SMLA_OK) return st;
+  // compressed keys under the causal mask need cmp_residual_k, which this
+  // entry point has no argument for
+  if (desc->cmp_ratio != 1 && desc->mask_mode == 3) return SMLA_ERR_UNSUPPORTED;
   if (s.n_items > kMaxItems) return SMLA_ERR_CAPACITY;  // before any CUDA call
   if (s.n_tokens == 0 || s.width == 0) return SMLA_OK;
   if (q == nullptr || softmax_lse == nullptr || out == nullptr) return SMLA_ERR_NULLPTR;
@@ -210,6 +213,7 @@ extern "C" smla_status smla_l1norm_run_noalloc(const smla_l1norm_desc* desc, con
   p.topk = s.sparse ? desc->topk : 0;
   p.width = s.width;
   p.mask_mode = desc->mask_mode;
+  p.cmp_ratio = desc->cmp_ratio;
   p.stages = ls.stages;
   p.idesc = static_cast<int32_t>(smla::make_idesc(desc->dtype, s.n_mma));
   p.idesc_lse = static_cast<int32_t>(smla::make_idesc(desc->dtype, smla::kTileKeys));

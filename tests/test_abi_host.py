@@ -53,7 +53,6 @@ BASE = dict(layout="BSND", dtype="bf16", num_heads_q=8, batch_size=1, max_seqlen
     (dict(head_dim=256), smla.SMLA_ERR_INVALID),           # D only 512
     (dict(mask_mode=2), smla.SMLA_ERR_UNSUPPORTED),
     (dict(mask_mode=5), smla.SMLA_ERR_INVALID),
-    (dict(cmp_ratio=4), smla.SMLA_ERR_UNSUPPORTED),        # compressed keys not built
     (dict(cmp_ratio=0), smla.SMLA_ERR_INVALID),
     (dict(cmp_ratio=129), smla.SMLA_ERR_INVALID),
     (dict(dtype=7), smla.SMLA_ERR_INVALID),
@@ -140,6 +139,24 @@ def test_key_ring_depth_is_even_for_every_head_count(topk):
                                         has_topk_length=False, softmax_scale=0.05)
         assert info.stages % 2 == 0 and 4 <= info.stages <= 12, (G, info.stages)
         assert info.smem_bytes <= 232448
+
+
+def test_compressed_keys_are_accepted_and_bound_the_dense_tiles():
+    """cmp_ratio 2..128 is accepted.  The host does not see cmp_residual_k
+    (a device tensor), so dense work items are sized for the largest
+    residual, c - 1: key j of row r counts when j*c + c - 1 <= r + Sk*c + c - 1 - Sq."""
+    S1, Sk, c = 64, 40, 8
+    items, _, info = smla.schedule_host(4, num_heads_q=16, batch_size=1, max_seqlen_q=S1, max_seqlen_k=Sk,
+                                        topk=0, mask_mode=3, softmax_scale=0.05, cmp_ratio=c)
+    assert info.out_width == Sk
+    for q_tok, nrows, r0, k_base, Sq, Sk_, ntiles, _ in items:
+        last = r0 + nrows - 1
+        vis = min(Sk, max(0, last + Sk * c + (c - 1) - S1 + 1) // c)
+        assert ntiles == -(-vis // 128)
+    _, _, info = smla.schedule_host(4, want_items=False, num_heads_q=8, batch_size=1, max_seqlen_q=16,
+                                    max_seqlen_k=300, topk=64, mask_mode=3, softmax_scale=0.05, cmp_ratio=128,
+                                    has_topk_length=True)
+    assert info.num_items == 16
 
 
 def test_mma_issuers_follow_the_accumulator_width():

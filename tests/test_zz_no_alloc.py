@@ -39,6 +39,18 @@ def _call_noalloc(lib, torch, w, t, out):
     return code
 
 
+def test_compressed_keys_under_the_causal_mask_are_not_taken():
+    """cmp_residual_k has no argument in the allocation-free entry point, so
+    compressed keys with mask_mode 3 are rejected there (before any CUDA
+    call); plans take them through smla_l1norm_run_tensors."""
+    lib = smla.library()
+    d, keep = smla._make_desc(layout="BSND", dtype="bf16", num_heads_q=8, batch_size=1, max_seqlen_q=16,
+                              max_seqlen_k=64, topk=8, mask_mode=3, cmp_ratio=4, softmax_scale=1.0)
+    assert lib.smla_l1norm_run_noalloc(ctypes.byref(d), None, None, None, None, None, None, None) == \
+        smla.SMLA_ERR_UNSUPPORTED
+    del keep
+
+
 def test_capacity_rejected_before_any_cuda_call():
     """More work items than the fixed scratch holds: SMLA_ERR_CAPACITY, with
     no CUDA call (this runs on a host without a GPU)."""
@@ -91,7 +103,7 @@ def test_noalloc_config_counts_items_and_ctas():
     (dict(num_heads_k=2), smla.SMLA_ERR_INVALID),
     (dict(head_dim=256), smla.SMLA_ERR_INVALID),
     (dict(mask_mode=2), smla.SMLA_ERR_UNSUPPORTED),
-    (dict(cmp_ratio=4), smla.SMLA_ERR_UNSUPPORTED),
+    (dict(cmp_ratio=0), smla.SMLA_ERR_INVALID),
     (dict(layout="TND"), smla.SMLA_ERR_NULLPTR),
     (dict(topk=0), smla.SMLA_ERR_INVALID),
 ])
