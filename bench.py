@@ -467,7 +467,8 @@ def other_config_line(smla, n, steps, device, stream, flush):
             "north_star_roofline": north_star_block(sum(bytes_.values()), sec, hbm_gbs,
                                                     flops / (bf16_tf * 1e12)),
             "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "num_items", "stages",
-                                                                            "mma_n", "rows_per_item", "mma_issuers")}}
+                                                                            "mma_n", "rows_per_item", "mma_issuers",
+                                                                            "cta_pairs")}}
     del plan, dev, out
     torch.cuda.empty_cache()
     return line
@@ -666,7 +667,8 @@ def run_ours(args, world, rank, local):
         "wall_s_timed_region": wall,
         "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "stages", "mma_n",
                                                                         "smem_bytes", "max_cta_cost",
-                                                                        "mean_cta_cost", "mma_issuers")},
+                                                                        "mean_cta_cost", "mma_issuers",
+                                                                        "cta_pairs")},
     }
     print(json.dumps(line), flush=True)
     return 0

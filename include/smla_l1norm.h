@@ -156,6 +156,9 @@ typedef struct {
   int32_t mma_issuers;     /* threads issuing the L1-norm launch's MMAs: 4 when
                               the sparse form's N is at most 64 (each owns a
                               quarter of the head dimension), else 2          */
+  int32_t cta_pairs;       /* 2-CTA clusters of the CTA-pair L1-norm launch
+                              (sparse form, N = 128: one MMA covers both CTAs'
+                              keys); 0 = the single-CTA kernel runs it        */
 } smla_plan_info;
 
 /*

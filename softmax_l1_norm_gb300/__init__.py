@@ -63,7 +63,7 @@ class PlanInfo(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32), ("out_width", ctypes.c_int32), ("est_tiles", ctypes.c_int64),
         ("max_cta_cost", ctypes.c_double), ("mean_cta_cost", ctypes.c_double),
         ("q_rows_total", ctypes.c_int64), ("k_rows_total", ctypes.c_int64),
-        ("host_chunks", ctypes.c_int32), ("mma_issuers", ctypes.c_int32),
+        ("host_chunks", ctypes.c_int32), ("mma_issuers", ctypes.c_int32), ("cta_pairs", ctypes.c_int32),
     ]
 
     def as_dict(self):

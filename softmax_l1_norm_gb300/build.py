@@ -19,7 +19,7 @@ LIB = os.path.join(BUILD, "libsmla_l1norm.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["smla_kernel.cu", "smla_api.cpp", "smla_noalloc.cu"]
+SOURCES = ["smla_kernel.cu", "smla_pair.cu", "smla_api.cpp", "smla_noalloc.cu"]
 
 
 def _nvcc() -> str:

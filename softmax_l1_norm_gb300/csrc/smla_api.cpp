@@ -156,7 +156,7 @@ struct Schedule {
 // time.  Cost of an item: its 128-key tiles, plus a per-token overhead for
 // the q load and the zero tail.
 Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ctas, int64_t tok_lo = 0,
-                        int64_t tok_hi = INT64_MAX) {
+                        int64_t tok_hi = INT64_MAX, bool pair = false) {
   Schedule s;
   std::vector<WorkItem> items;
   std::vector<double> cost;
@@ -180,7 +180,8 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
         WorkItem w{static_cast<int32_t>(tok), 1, static_cast<int32_t>(r), static_cast<int32_t>(g.k0[b]),
                    static_cast<int32_t>(Sq), static_cast<int32_t>(Sk), 0, b};
         items.push_back(w);
-        cost.push_back(static_cast<double>(tiles) + row_overhead +
+        // a CTA pair runs two tiles per step
+        cost.push_back(static_cast<double>(pair ? ceil_div(tiles, 2) : tiles) + row_overhead +
                        0.02 * static_cast<double>(g.width - tiles * smla::kTileKeys) / smla::kTileKeys);
         s.est_tiles += tiles;
       }
@@ -264,16 +265,16 @@ int stages_for(int n_mma, int smem_limit) {
   return st;
 }
 
-uint32_t make_idesc(int dtype, int n_mma) {
+uint32_t make_idesc(int dtype, int n_mma, int m) {
   // tcgen05 instruction descriptor, kind::f16: fp32 accumulator, A and B of
-  // the same 16-bit type, both K-major, M = 128, N = n_mma.
+  // the same 16-bit type, both K-major, M = m, N = n_mma.
   const uint32_t ab = dtype == SMLA_DTYPE_BF16 ? 1u : 0u;
   uint32_t d = 0;
   d |= 1u << 4;                                    // D format: f32
   d |= ab << 7;                                    // A format
   d |= ab << 10;                                   // B format
   d |= static_cast<uint32_t>(n_mma >> 3) << 17;    // N / 8
-  d |= static_cast<uint32_t>(128 >> 4) << 24;      // M / 16
+  d |= static_cast<uint32_t>(m >> 4) << 24;        // M / 16
   return d;
 }
 
@@ -340,6 +341,11 @@ struct smla_plan {
   smla_plan_info info{};
   int64_t timeout_ns = 0;
   int32_t withhold_q = 0;            // test hook (SMLA_DEBUG_WITHHOLD_Q)
+  // CTA-pair L1-norm launch (sparse, N = 128): clusters (0 = not used), its
+  // ring depth and shared memory, and its own work list (one per cluster)
+  int pair_clusters = 0, pair_stages = 0, pair_smem = 0;
+  int32_t* d_pair_begin = nullptr;
+  WorkItem* d_pair_items = nullptr;
   std::vector<WorkItem> items_host;  // the work list as uploaded, for the gather test hook
   // run_from_host pipeline: token chunks, each with its own work schedule,
   // so that the copies of one chunk overlap the kernel of the previous one
@@ -449,7 +455,33 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
       cs.push_back(build_schedule(desc, g, ctas, plan->chunk_lo[c], plan->chunk_hi[c]));
   }
 
+  // CTA pairs for the L1-norm launch (sparse form, N = 128).  The pair
+  // kernel splits each token's tiles between two SMs, so it pays off when
+  // tokens are long: measured on GB300, 0.79 vs 0.72 of the bf16 peak with
+  // 32768 tokens of top-2048 (15.9 tiles a token), but 0.53 vs 0.61 with
+  // 4096 causal tokens (12.3 tiles a token).  It runs when the schedule's
+  // mean is at least kPairMinTiles tiles a token; SMLA_PAIR=0 / 1 forces the
+  // choice.  As many clusters as fit on the device at once.
+  constexpr double kPairMinTiles = 14.0;
+  Schedule ps;
+  const char* pair_env = std::getenv("SMLA_PAIR");
+  const int pair_force = pair_env == nullptr ? -1 : (std::atoi(pair_env) != 0 ? 1 : 0);
+  const double mean_tiles = static_cast<double>(s.est_tiles) / static_cast<double>(std::max<int64_t>(1, g.n_tokens));
+  const bool want_pair = pair_force == 1 || (pair_force == -1 && mean_tiles >= kPairMinTiles);
+  if (g.sparse && g.n_mma == 128 && want_pair) {
+    int clusters = 0;
+    if (smla::configure_pair(optin, &clusters) == cudaSuccess && clusters > 0) {
+      clusters = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(clusters, std::max<int64_t>(1, g.n_tokens))));
+      plan->pair_clusters = clusters;
+      plan->pair_stages = smla::pair_stages(optin);
+      plan->pair_smem = smla::pair_smem_bytes(plan->pair_stages);
+      ps = build_schedule(desc, g, clusters, 0, INT64_MAX, true);
+    }
+    cudaGetLastError();  // a device without clusters of two: the single-CTA kernel
+  }
+
   // one device buffer: status word | CTA offsets | work items | per chunk: CTA offsets | work items
+  // | pair CTA offsets | pair work items
   auto round256 = [](size_t n) { return ((n + 255) / 256) * 256; };
   const size_t off_begin = 256;
   const size_t off_items = off_begin + round256(s.cta_begin.size() * sizeof(int32_t));
@@ -461,6 +493,10 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
     off_ci.push_back(bytes);
     bytes += round256(std::max<size_t>(1, c.items.size()) * sizeof(WorkItem));
   }
+  const size_t off_pb = bytes;
+  bytes += round256(std::max<size_t>(1, ps.cta_begin.size()) * sizeof(int32_t));
+  const size_t off_pi = bytes;
+  bytes += round256(std::max<size_t>(1, ps.items.size()) * sizeof(WorkItem));
   e = cudaMalloc(&plan->dbuf, bytes);
   if (e != cudaSuccess) {
     release_plan(plan);
@@ -474,6 +510,9 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
     if (!cs[c].items.empty())
       std::memcpy(host.data() + off_ci[c], cs[c].items.data(), cs[c].items.size() * sizeof(WorkItem));
   }
+  if (!ps.cta_begin.empty())
+    std::memcpy(host.data() + off_pb, ps.cta_begin.data(), ps.cta_begin.size() * sizeof(int32_t));
+  if (!ps.items.empty()) std::memcpy(host.data() + off_pi, ps.items.data(), ps.items.size() * sizeof(WorkItem));
   e = cudaMemcpy(plan->dbuf, host.data(), bytes, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = smla::configure_fused_for_device();
   if (e == cudaSuccess && !cs.empty()) {
@@ -494,6 +533,9 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   plan->d_status = reinterpret_cast<int32_t*>(b);
   plan->d_cta_begin = reinterpret_cast<int32_t*>(b + off_begin);
   plan->d_items = reinterpret_cast<WorkItem*>(b + off_items);
+  plan->d_pair_begin = reinterpret_cast<int32_t*>(b + off_pb);
+  plan->d_pair_items = reinterpret_cast<WorkItem*>(b + off_pi);
+  plan->info.cta_pairs = plan->pair_clusters;
   plan->info.host_chunks = static_cast<int32_t>(cs.size());
   for (size_t c = 0; c < cs.size(); ++c) {
     plan->d_chunk_begin.push_back(reinterpret_cast<int32_t*>(b + off_cb[c]));
@@ -585,8 +627,10 @@ smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, flo
   for (const void* a : a4)
     if (a != nullptr && !aligned4(a)) return SMLA_ERR_INVALID;
 
+  // the CTA-pair kernel runs the whole-problem L1-norm launch when the plan has it
+  const bool pair = mode == smla::kModeL1 && chunk < 0 && plan->pair_clusters > 0;
   CUtensorMap tq;
-  const int q_box = g.R * g.G;
+  const int q_box = pair ? g.G / 2 : g.R * g.G;
   if (!smla::encode_rows_map(&tq, t->q, g.q_rows, q_box, plan->desc.dtype)) {
     g_last_cuda_error = "cuTensorMapEncodeTiled(q) failed";
     return SMLA_ERR_CUDA;
@@ -619,6 +663,16 @@ smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, flo
   p.inv_g = 1.0f / static_cast<float>(g.G);
   p.timeout_ns = plan->timeout_ns;
   p.withhold_q = plan->withhold_q;
+  if (pair) {
+    p.items = plan->d_pair_items;
+    p.cta_begin = plan->d_pair_begin;
+    p.stages = plan->pair_stages;
+    p.idesc = static_cast<int32_t>(smla::make_idesc(plan->desc.dtype, g.n_mma, 256));
+    cudaError_t e = smla::launch_pair(p, tq, plan->pair_clusters, plan->pair_smem,
+                                      reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pair kernel launch");
+    return SMLA_OK;
+  }
   const int issuers = mode == smla::kModeL1 ? smla::l1_issuers(g) : 2;
   cudaError_t e = smla::launch_fused(p, tq, g.sparse, mode, issuers, plan->num_ctas, plan->smem,
                                      reinterpret_cast<cudaStream_t>(stream));

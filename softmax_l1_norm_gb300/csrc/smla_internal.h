@@ -152,8 +152,19 @@ int stages_for(int n_mma, int smem_limit);
 // is unchanged: with two producer groups filling their stages in order, an
 // even depth keeps every barrier within one phase for two or four issuers.
 inline int l1_issuers(const Shape& s) { return (s.sparse && s.n_mma <= kAccCols / 4) ? 4 : 2; }
-// tcgen05 instruction descriptor, kind::f16, M = 128, N = n_mma.
-uint32_t make_idesc(int dtype, int n_mma);
+// tcgen05 instruction descriptor, kind::f16, M = m (128, or 256 for a CTA
+// pair), N = n_mma.
+uint32_t make_idesc(int dtype, int n_mma, int m = 128);
+
+// The CTA-pair L1-norm kernel (smla_pair.cu): sparse form with N = 128.
+// Shared memory for a ring of `stages`, the deepest even ring that fits,
+// the device set-up (shared-memory cap; how many 2-CTA clusters fit at once)
+// and the launch (grid = 2 * clusters).
+int pair_smem_bytes(int stages);
+int pair_stages(int smem_limit);
+cudaError_t configure_pair(int smem_optin, int* max_clusters);
+cudaError_t launch_pair(const KernelParams& p, const CUtensorMap& tmap_q, int clusters, int smem_bytes,
+                        cudaStream_t stream);
 // 2-D (rows x 512) SWIZZLE_128B tensor map of a half-precision tensor, boxes
 // of 64 columns x box_rows rows.
 bool encode_rows_map(CUtensorMap* map, const void* ptr, int64_t rows, int box_rows, int dtype);

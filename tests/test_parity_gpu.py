@@ -237,6 +237,33 @@ def test_wait_timeout_probe_reports_and_returns(lib):
     assert float(x.sum()) == 4.0
 
 
+@pytest.mark.parametrize("topk,S2,mask", [(300, 700, 3), (128, 400, 0), (2048, 2100, 3)])
+def test_cta_pair_kernel(lib, monkeypatch, topk, S2, mask):
+    """Sparse form with 128 heads: the L1-norm launch runs on 2-CTA clusters
+    (one MMA over both CTAs' keys; forced here, chosen by the plan for long
+    tokens).  Odd and even tile counts per token,
+    tokens whose causal limit cuts the tiles; compared with the oracle
+    element by element and with the single-CTA kernel (SMLA_PAIR=0)."""
+    w = W.make_workload(layout="BSND", dtype="bf16", B=2, S1=40, S2=S2, G=128, topk=topk, mask_mode=mask,
+                        seed=7000 + topk, lse=None)
+    exact_lse(oracle, w)
+    want = oracle.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **oracle_kwargs(w))
+    t = to_device(w)
+    monkeypatch.setenv("SMLA_PAIR", "1")   # these tokens are short: the plan would pick one CTA
+    got, plan, _, status = run_gpu(lib, w, tensors=t)
+    assert plan.info.cta_pairs > 0 and status[0] == lib.SMLA_OK
+    assert_close(got, want, what="CTA pair kernel")
+    rows = got.reshape(w.n_tokens, -1).astype(np.float64)
+    assert np.all(rows[invalid_slot_mask(w)] == 0.0)
+    assert np.all(np.abs(rows.sum(axis=1) - 1.0) <= ROWSUM_TOL)
+    monkeypatch.setenv("SMLA_PAIR", "0")
+    single, plan1, _, _ = run_gpu(lib, w, tensors=t)
+    assert plan1.info.cta_pairs == 0
+    assert_close(single, want, what="single-CTA kernel")
+    again, _, _, _ = run_gpu(lib, w, plan=plan, tensors=t)
+    assert np.array_equal(again.view(np.uint32), got.view(np.uint32)), "pair kernel run to run"
+
+
 def test_fused_kernel_waits_give_up_and_report(lib, monkeypatch):
     """A plan whose launches never load one q chunk (a test hook) and whose
     device waits are bounded by 30 ms: the MMA issuers' wait for that chunk
@@ -310,11 +337,13 @@ def sampled_parity(lib, n, n_sample=24, seed=0):
     return w, got_rows
 
 
-def test_config3_dsv32_full_size_every_row(lib, tmp_path):
+def test_config3_dsv32_full_size_every_row(lib, tmp_path, monkeypatch):
     """The 4096-token, 128-head, top-2048 causal workload at full size, in the
     benchmark's launch configuration: the exact forward LSE is planted on
     every row and every one of the 8.4 M output elements is compared with the
-    oracle; every row sums to 1 within 1e-3 and masked slots are exactly 0."""
+    oracle; every row sums to 1 within 1e-3 and masked slots are exactly 0.
+    Then the same with the CTA-pair kernel forced (the plan picks the
+    single-CTA kernel for this workload)."""
     import oracle_pool
     w = W.make_config(3)
     n_tok = w.n_tokens
@@ -322,11 +351,16 @@ def test_config3_dsv32_full_size_every_row(lib, tmp_path):
     W.set_lse_rows(w, lse)
     got, plan, t, status = run_gpu(lib, w)
     assert status[0] == lib.SMLA_OK and plan.info.num_ctas == torch.cuda.get_device_properties(0).multi_processor_count
-    got_rows = got.reshape(n_tok, -1)
-    assert_close(got_rows, want, what="config 3, every element")
-    sums = got_rows.astype(np.float64).sum(axis=1)
-    assert np.all(np.abs(sums - 1.0) <= ROWSUM_TOL), (sums.min(), sums.max())
-    assert np.all(got_rows[invalid_slot_mask(w)] == 0.0)
+    assert plan.info.cta_pairs == 0
+    monkeypatch.setenv("SMLA_PAIR", "1")
+    got_pair, plan_pair, _, status = run_gpu(lib, w, tensors=t)
+    assert status[0] == lib.SMLA_OK and plan_pair.info.cta_pairs > 0
+    for name, g in (("single-CTA", got), ("CTA-pair", got_pair)):
+        got_rows = g.reshape(n_tok, -1)
+        assert_close(got_rows, want, what=f"config 3, every element, {name} kernel")
+        sums = got_rows.astype(np.float64).sum(axis=1)
+        assert np.all(np.abs(sums - 1.0) <= ROWSUM_TOL), (name, sums.min(), sums.max())
+        assert np.all(got_rows[invalid_slot_mask(w)] == 0.0)
 
 
 def test_config4_varlen_tnd_full_size_sampled(lib):
