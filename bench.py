@@ -468,7 +468,8 @@ def other_config_line(smla, n, steps, device, stream, flush):
                                                     flops / (bf16_tf * 1e12)),
             "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "num_items", "stages",
                                                                             "mma_n", "rows_per_item", "mma_issuers",
-                                                                            "cta_pairs")}}
+                                                                            "cta_pairs", "split_tiles",
+                                                                            "split_items")}}
     del plan, dev, out
     torch.cuda.empty_cache()
     return line
@@ -668,7 +669,7 @@ def run_ours(args, world, rank, local):
         "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "stages", "mma_n",
                                                                         "smem_bytes", "max_cta_cost",
                                                                         "mean_cta_cost", "mma_issuers",
-                                                                        "cta_pairs")},
+                                                                        "cta_pairs", "split_tiles", "split_items")},
     }
     print(json.dumps(line), flush=True)
     return 0

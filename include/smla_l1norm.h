@@ -159,6 +159,12 @@ typedef struct {
   int32_t cta_pairs;       /* 2-CTA clusters of the CTA-pair L1-norm launch
                               (sparse form, N = 128: one MMA covers both CTAs'
                               keys); 0 = the single-CTA kernel runs it        */
+  int32_t split_tiles;     /* dense form: the L1-norm launch splits each token
+                              pack's keys into parts of at most this many
+                              128-key tiles (output slots depend on one key
+                              each, so the parts are independent); 0 = one
+                              part per pack                                 */
+  int64_t split_items;     /* work items of that split launch (0 = no split) */
 } smla_plan_info;
 
 /*
@@ -343,14 +349,20 @@ smla_status smla_l1norm_get_status(const smla_plan *plan, smla_stream_t stream, 
 /*
  * Host-only view of the scheduler, for inspection and tests: validate
  * ``desc`` and build the schedule for ``num_ctas`` CTAs without any CUDA
- * call.  If ``items`` is non-NULL it receives up to ``items_capacity`` work
- * items of 8 int32 each, grouped by CTA (fields: first token, tokens in the
- * item, local row of the first token, first key row of the sequence, Sq, Sk,
- * key tiles of a dense item, sequence number b); ``cta_offsets`` (num_ctas + 1 int32)
- * receives where each CTA's items start.  ``info`` receives the summary.
+ * call.  ``split_tiles``: 0 = whole token packs (the schedule of every launch
+ * but the dense L1-norm one); n > 0 = dense packs split into parts of at most
+ * n key tiles (SMLA_ERR_INVALID for the sparse form); -1 = what a plan's
+ * dense L1-norm launch runs (split or not, as the plan would choose).  If
+ * ``items`` is non-NULL it receives up to ``items_capacity`` work items of 12
+ * int32 each, grouped by CTA (fields: first token, tokens in the item, local
+ * row of the first token, first key row of the sequence, Sq, Sk, key tiles of
+ * a dense item, sequence number b, first key tile, cut_tail (1: an earlier
+ * part of a split pack, which zeroes only its own key range), two reserved
+ * zeros); ``cta_offsets`` (num_ctas + 1 int32) receives where each CTA's items
+ * start.  ``info`` receives the summary, with the split chosen.
  */
 smla_status smla_l1norm_schedule_host(const smla_l1norm_desc *desc, int32_t num_ctas,
-                                      int32_t *items, int64_t items_capacity,
+                                      int32_t split_tiles, int32_t *items, int64_t items_capacity,
                                       int32_t *cta_offsets, smla_plan_info *info);
 
 /*

@@ -64,6 +64,7 @@ class PlanInfo(ctypes.Structure):
         ("max_cta_cost", ctypes.c_double), ("mean_cta_cost", ctypes.c_double),
         ("q_rows_total", ctypes.c_int64), ("k_rows_total", ctypes.c_int64),
         ("host_chunks", ctypes.c_int32), ("mma_issuers", ctypes.c_int32), ("cta_pairs", ctypes.c_int32),
+        ("split_tiles", ctypes.c_int32), ("split_items", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -123,7 +124,7 @@ def library():
     lib.smla_l1norm_run_from_host.restype = I32
     lib.smla_l1norm_get_status.argtypes = [P, P, ctypes.POINTER(I32)]
     lib.smla_l1norm_get_status.restype = I32
-    lib.smla_l1norm_schedule_host.argtypes = [ctypes.POINTER(_Desc), I32, P, I64, P, ctypes.POINTER(PlanInfo)]
+    lib.smla_l1norm_schedule_host.argtypes = [ctypes.POINTER(_Desc), I32, I32, P, I64, P, ctypes.POINTER(PlanInfo)]
     lib.smla_l1norm_schedule_host.restype = I32
     lib.smla_status_string.argtypes = [I32]
     lib.smla_status_string.restype = ctypes.c_char_p
@@ -179,22 +180,27 @@ def _make_desc(*, layout="BSND", dtype="bf16", num_heads_q, num_heads_k=1, head_
     return d, keep
 
 
-def schedule_host(num_ctas: int, want_items: bool = True, **desc_kwargs):
+ITEM_FIELDS = 12
+
+
+def schedule_host(num_ctas: int, want_items: bool = True, split_tiles: int = 0, **desc_kwargs):
     """Host-only scheduler view (no CUDA call): returns (items, cta_offsets, info)
-    with items an (n, 8) int32 list-of-lists grouped by CTA."""
+    with items an (n, 12) int32 list-of-lists grouped by CTA.  ``split_tiles``:
+    0 whole packs, n > 0 dense packs split into parts of n key tiles, -1 the
+    dense L1-norm launch's own choice."""
     lib = library()
     d, keep = _make_desc(**desc_kwargs)
     info = PlanInfo()
-    code = lib.smla_l1norm_schedule_host(ctypes.byref(d), num_ctas, None, 0, None, ctypes.byref(info))
+    code = lib.smla_l1norm_schedule_host(ctypes.byref(d), num_ctas, split_tiles, None, 0, None, ctypes.byref(info))
     _check(code, "smla_l1norm_schedule_host")
     if not want_items:
         return None, None, info
     n = info.num_items
-    items = (ctypes.c_int32 * (8 * max(1, n)))()
+    items = (ctypes.c_int32 * (ITEM_FIELDS * max(1, n)))()
     offs = (ctypes.c_int32 * (num_ctas + 1))()
-    code = lib.smla_l1norm_schedule_host(ctypes.byref(d), num_ctas, items, n, offs, ctypes.byref(info))
+    code = lib.smla_l1norm_schedule_host(ctypes.byref(d), num_ctas, split_tiles, items, n, offs, ctypes.byref(info))
     _check(code, "smla_l1norm_schedule_host")
-    rows = [list(items[8 * i: 8 * i + 8]) for i in range(n)]
+    rows = [list(items[ITEM_FIELDS * i: ITEM_FIELDS * i + ITEM_FIELDS]) for i in range(n)]
     del keep
     return rows, list(offs), info
 

@@ -156,7 +156,7 @@ struct Schedule {
 // time.  Cost of an item: its 128-key tiles, plus a per-token overhead for
 // the q load and the zero tail.
 Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ctas, int64_t tok_lo = 0,
-                        int64_t tok_hi = INT64_MAX, bool pair = false) {
+                        int64_t tok_hi = INT64_MAX, bool pair = false, int64_t split = 0) {
   Schedule s;
   std::vector<WorkItem> items;
   std::vector<double> cost;
@@ -191,12 +191,23 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
         const int64_t nrows = std::min<int64_t>(g.R, Sq - r0);
         const int64_t vis = visible_keys(r0 + nrows - 1, Sq, Sk, d->mask_mode, d->cmp_ratio);
         const int64_t tiles = ceil_div(std::min<int64_t>(vis, g.width), smla::kTileKeys);
-        WorkItem w{static_cast<int32_t>(g.q0[b] + r0), static_cast<int32_t>(nrows), static_cast<int32_t>(r0),
-                   static_cast<int32_t>(g.k0[b]), static_cast<int32_t>(Sq), static_cast<int32_t>(Sk),
-                   static_cast<int32_t>(tiles), b};
-        items.push_back(w);
-        cost.push_back(static_cast<double>(tiles) + row_overhead +
-                       0.02 * nrows * static_cast<double>(g.width - tiles * smla::kTileKeys) / smla::kTileKeys);
+        // one item, or (split > 0) as few parts of at most `split` key tiles
+        // as cover the pack, of equal size to within one tile; the last part
+        // (or the only one) zeroes the rest of the rows
+        const int64_t nparts = split > 0 ? std::max<int64_t>(1, ceil_div(tiles, split)) : 1;
+        const int64_t part = std::max<int64_t>(1, ceil_div(tiles, nparts));
+        for (int64_t t0 = 0; t0 == 0 || t0 < tiles; t0 += part) {
+          const int64_t n = std::min<int64_t>(part, tiles - t0);
+          const bool last = t0 + part >= tiles;
+          WorkItem w{static_cast<int32_t>(g.q0[b] + r0), static_cast<int32_t>(nrows), static_cast<int32_t>(r0),
+                     static_cast<int32_t>(g.k0[b]), static_cast<int32_t>(Sq), static_cast<int32_t>(Sk),
+                     static_cast<int32_t>(std::max<int64_t>(n, 0)), b};
+          w.t0 = static_cast<int32_t>(t0);
+          w.cut_tail = last ? 0 : 1;
+          items.push_back(w);
+          const double tail = last ? static_cast<double>(g.width - tiles * smla::kTileKeys) / smla::kTileKeys : 0.0;
+          cost.push_back(static_cast<double>(std::max<int64_t>(n, 0)) + row_overhead + 0.02 * nrows * tail);
+        }
         s.est_tiles += tiles;
       }
     }
@@ -232,6 +243,36 @@ Schedule build_schedule(const smla_l1norm_desc* d, const Geometry& g, int num_ct
     s.mean_cost = std::accumulate(load.begin(), load.end(), 0.0) / num_ctas;
   }
   return s;
+}
+
+// Dense form: when a few long token packs would leave most CTAs waiting for
+// the heaviest (few packs, many key tiles each), the L1-norm launch splits
+// each pack's key tiles into parts of at most `split` tiles, which the
+// scheduler deals out separately; a part reloads its pack's q block.  The
+// part size chosen is the one whose schedule has the lightest heaviest CTA,
+// kept when it beats the unsplit schedule `base` by at least 10 %; 0 = no
+// split.  `force` (the SMLA_SPLIT variable, may be null) fixes the part size
+// (0: no split).  The forward-LSE launches reduce over a row's keys and always
+// take whole packs.
+int64_t choose_split(const smla_l1norm_desc* d, const Geometry& g, int num_ctas, const Schedule& base,
+                     const char* force) {
+  if (g.sparse) return 0;
+  int64_t max_tiles = 0;
+  for (const WorkItem& w : base.items) max_tiles = std::max<int64_t>(max_tiles, w.ntiles);
+  int64_t best = 0;
+  if (force != nullptr) {
+    best = std::max<int64_t>(0, std::atoll(force));
+  } else if (max_tiles > 1 && static_cast<int64_t>(base.items.size()) < 8 * static_cast<int64_t>(num_ctas)) {
+    double best_cost = 0.9 * base.max_cost;
+    for (int64_t cap = 1; cap < max_tiles; cap = cap < 4 ? cap + 1 : cap * 2) {
+      const Schedule t = build_schedule(d, g, num_ctas, 0, INT64_MAX, false, cap);
+      if (t.max_cost < best_cost) {
+        best_cost = t.max_cost;
+        best = cap;
+      }
+    }
+  }
+  return (best > 0 && best < max_tiles) ? best : 0;
 }
 
 void fill_info(const Geometry& g, const Schedule& s, int num_ctas, int stages, int smem, smla_plan_info* info) {
@@ -346,6 +387,11 @@ struct smla_plan {
   int pair_clusters = 0, pair_stages = 0, pair_smem = 0;
   int32_t* d_pair_begin = nullptr;
   WorkItem* d_pair_items = nullptr;
+  // Dense L1-norm launch split along the keys (0 = not split): parts of at
+  // most split_tiles key tiles, with their own work list
+  int split_tiles = 0;
+  int32_t* d_split_begin = nullptr;
+  WorkItem* d_split_items = nullptr;
   std::vector<WorkItem> items_host;  // the work list as uploaded, for the gather test hook
   // run_from_host pipeline: token chunks, each with its own work schedule,
   // so that the copies of one chunk overlap the kernel of the previous one
@@ -372,13 +418,17 @@ void release_plan(smla_plan* plan) {
 
 extern "C" {
 
-smla_status smla_l1norm_schedule_host(const smla_l1norm_desc* desc, int32_t num_ctas, int32_t* items,
-                                      int64_t items_capacity, int32_t* cta_offsets, smla_plan_info* info) {
+smla_status smla_l1norm_schedule_host(const smla_l1norm_desc* desc, int32_t num_ctas, int32_t split_tiles,
+                                      int32_t* items, int64_t items_capacity, int32_t* cta_offsets,
+                                      smla_plan_info* info) {
   Geometry g;
   smla_status st = validate(desc, &g);
   if (st != SMLA_OK) return st;
   if (num_ctas <= 0) return SMLA_ERR_INVALID;
-  const Schedule s = build_schedule(desc, g, num_ctas);
+  const Schedule base = build_schedule(desc, g, num_ctas);
+  const int64_t split = split_tiles < 0 ? choose_split(desc, g, num_ctas, base, nullptr) : split_tiles;
+  if (g.sparse && split > 0) return SMLA_ERR_INVALID;
+  const Schedule s = split > 0 ? build_schedule(desc, g, num_ctas, 0, INT64_MAX, false, split) : base;
   if (items != nullptr) {
     const int64_t n = std::min<int64_t>(items_capacity, static_cast<int64_t>(s.items.size()));
     std::memcpy(items, s.items.data(), static_cast<size_t>(n) * sizeof(WorkItem));
@@ -387,6 +437,8 @@ smla_status smla_l1norm_schedule_host(const smla_l1norm_desc* desc, int32_t num_
   if (info != nullptr) {
     const int stages = smla::stages_for(g.n_mma, kDefaultSmemOptin);
     fill_info(g, s, num_ctas, stages, smla::smem_bytes_for(g.n_mma, stages), info);
+    info->split_tiles = static_cast<int32_t>(split);
+    info->split_items = split > 0 ? static_cast<int64_t>(s.items.size()) : 0;
   }
   return SMLA_OK;
 }
@@ -480,8 +532,18 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
     cudaGetLastError();  // a device without clusters of two: the single-CTA kernel
   }
 
+  // Dense form: the L1-norm launch may split token packs along the keys.
+  Schedule ss;
+  if (!g.sparse) {
+    const int64_t split = choose_split(desc, g, ctas, s, std::getenv("SMLA_SPLIT"));
+    if (split > 0) {
+      ss = build_schedule(desc, g, ctas, 0, INT64_MAX, false, split);
+      plan->split_tiles = static_cast<int>(split);
+    }
+  }
+
   // one device buffer: status word | CTA offsets | work items | per chunk: CTA offsets | work items
-  // | pair CTA offsets | pair work items
+  // | pair CTA offsets | pair work items | split CTA offsets | split work items
   auto round256 = [](size_t n) { return ((n + 255) / 256) * 256; };
   const size_t off_begin = 256;
   const size_t off_items = off_begin + round256(s.cta_begin.size() * sizeof(int32_t));
@@ -497,6 +559,10 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   bytes += round256(std::max<size_t>(1, ps.cta_begin.size()) * sizeof(int32_t));
   const size_t off_pi = bytes;
   bytes += round256(std::max<size_t>(1, ps.items.size()) * sizeof(WorkItem));
+  const size_t off_sb = bytes;
+  bytes += round256(std::max<size_t>(1, ss.cta_begin.size()) * sizeof(int32_t));
+  const size_t off_si = bytes;
+  bytes += round256(std::max<size_t>(1, ss.items.size()) * sizeof(WorkItem));
   e = cudaMalloc(&plan->dbuf, bytes);
   if (e != cudaSuccess) {
     release_plan(plan);
@@ -513,6 +579,9 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   if (!ps.cta_begin.empty())
     std::memcpy(host.data() + off_pb, ps.cta_begin.data(), ps.cta_begin.size() * sizeof(int32_t));
   if (!ps.items.empty()) std::memcpy(host.data() + off_pi, ps.items.data(), ps.items.size() * sizeof(WorkItem));
+  if (!ss.cta_begin.empty())
+    std::memcpy(host.data() + off_sb, ss.cta_begin.data(), ss.cta_begin.size() * sizeof(int32_t));
+  if (!ss.items.empty()) std::memcpy(host.data() + off_si, ss.items.data(), ss.items.size() * sizeof(WorkItem));
   e = cudaMemcpy(plan->dbuf, host.data(), bytes, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = smla::configure_fused_for_device();
   if (e == cudaSuccess && !cs.empty()) {
@@ -536,6 +605,10 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   plan->d_pair_begin = reinterpret_cast<int32_t*>(b + off_pb);
   plan->d_pair_items = reinterpret_cast<WorkItem*>(b + off_pi);
   plan->info.cta_pairs = plan->pair_clusters;
+  plan->d_split_begin = reinterpret_cast<int32_t*>(b + off_sb);
+  plan->d_split_items = reinterpret_cast<WorkItem*>(b + off_si);
+  plan->info.split_tiles = plan->split_tiles;
+  plan->info.split_items = plan->split_tiles > 0 ? static_cast<int64_t>(ss.items.size()) : 0;
   plan->info.host_chunks = static_cast<int32_t>(cs.size());
   for (size_t c = 0; c < cs.size(); ++c) {
     plan->d_chunk_begin.push_back(reinterpret_cast<int32_t*>(b + off_cb[c]));
@@ -544,10 +617,10 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   if (std::getenv("SMLA_LOG") != nullptr) {
     std::fprintf(stderr,
                  "[smla] plan: tokens=%lld items=%lld ctas=%d R=%d N=%d stages=%d smem=%d tiles=%lld "
-                 "max/mean cost=%.2f/%.2f\n",
+                 "max/mean cost=%.2f/%.2f pairs=%d split=%d (max cost %.2f)\n",
                  static_cast<long long>(g.n_tokens), static_cast<long long>(s.items.size()), ctas, g.R,
                  g.n_mma, plan->stages, plan->smem, static_cast<long long>(s.est_tiles), s.max_cost,
-                 s.mean_cost);
+                 s.mean_cost, plan->pair_clusters, plan->split_tiles, ss.max_cost);
   }
   *plan_out = plan;
   return SMLA_OK;
@@ -672,6 +745,10 @@ smla_status launch_mode(const smla_plan* plan, const smla_l1norm_tensors* t, flo
                                       reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pair kernel launch");
     return SMLA_OK;
+  }
+  if (mode == smla::kModeL1 && chunk < 0 && plan->split_tiles > 0) {
+    p.items = plan->d_split_items;
+    p.cta_begin = plan->d_split_begin;
   }
   const int issuers = mode == smla::kModeL1 ? smla::l1_issuers(g) : 2;
   cudaError_t e = smla::launch_fused(p, tq, g.sparse, mode, issuers, plan->num_ctas, plan->smem,

@@ -420,14 +420,20 @@ __device__ __forceinline__ int item_tiles(const KernelParams& p, const WorkItem&
   }
   tl = 0;
   if (p.seqused_q == nullptr && p.seqused_k == nullptr) return w.ntiles;
-  // keys visible to the item's last participating row, within the output width
+  // keys visible to the item's last participating row, within the output
+  // width, counted from the item's first key tile t0.  Cut lengths can show
+  // a row more keys than the full lengths the plan sized the item for (a
+  // shorter Sq moves the right-down diagonal right), so the last part of a
+  // pack (or a whole pack) runs to the visible end; an earlier part of a
+  // split pack stops at its own range.
   const EffLen e = effective_lengths(p, w);
   const int rows = min(w.nrows, e.Sq - w.r0);
   if (rows <= 0) return 0;
   int vis = e.Sk;
   if (p.mask_mode != 0) vis = causal_limit(p, w, e, w.r0 + rows - 1);
   vis = min(vis, p.width);
-  return (vis + kTileKeys - 1) / kTileKeys;
+  const int n = max((vis + kTileKeys - 1) / kTileKeys - w.t0, 0);
+  return w.cut_tail ? min(n, w.ntiles) : n;
 }
 
 // Passes over an item's key tiles: the LSE pass, the L1-norm pass, or both.
@@ -620,7 +626,7 @@ __device__ __forceinline__ void produce_keys(const KernelParams& p, int pw, int 
       if (kSparse) {
         jn[i] = slot < c.tl ? __ldg(p.idx + static_cast<int64_t>(c.w.q_tok) * p.topk + slot) : -1;
       } else {
-        jn[i] = slot;
+        jn[i] = c.w.t0 * kTileKeys + slot;  // key position (the item's key range starts at tile t0)
       }
     }
   };

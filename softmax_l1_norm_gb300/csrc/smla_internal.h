@@ -49,8 +49,16 @@ struct WorkItem {
   int32_t Sk;       // key length of the sequence
   int32_t ntiles;   // dense form: 128-key tiles to compute on full lengths (the rest is zero)
   int32_t b;        // batch entry (sequence) of the item
+  // Dense L1-norm launch split along the keys: the item covers key tiles
+  // t0 .. t0 + ntiles - 1 of its tokens.  Every output slot depends on one
+  // key only, so the parts of a token pack are independent.  The last part
+  // also zeroes the row past its tiles (cut_tail = 0); an earlier part
+  // zeroes only what its own tiles leave uncomputed (cut_tail = 1).
+  int32_t t0 = 0;
+  int32_t cut_tail = 0;
+  int32_t reserved0 = 0, reserved1 = 0;
 };
-static_assert(sizeof(WorkItem) == 32, "WorkItem is 32 bytes");
+static_assert(sizeof(WorkItem) == 48, "WorkItem is 48 bytes");
 
 struct KernelParams {
   const uint8_t* k;           // key rows, 1024 bytes each

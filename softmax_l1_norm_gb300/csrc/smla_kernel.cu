@@ -249,7 +249,7 @@ __device__ __forceinline__ void fused_body(const KernelParams& p, const CUtensor
           // the running maximum moves once per 16 columns (tree maximum) and
           // the sum is split over four chains.  The loop is kept rolled: the
           // warps of all roles share the instruction cache.
-          const int lim = limit - t * kTileKeys;  // dense form: columns c < lim are kept
+          const int lim = limit - (w.t0 + t) * kTileKeys;  // dense form: columns c < lim are kept
           // Column pairs go through packed f32x2 add / mul (each lane rounded
           // as the scalar instruction rounds it).
           auto lse16 = [&](const uint32_t (&fa)[16], const uint32_t (&ga)[16], int c0, uint32_t bits16) {
@@ -338,7 +338,7 @@ __device__ __forceinline__ void fused_body(const KernelParams& p, const CUtensor
         wg_sync(bar_id);
       }
       for (int t = 0; t < nt; ++t, ++acc) {
-        const int slot = t * kTileKeys + et;
+        const int slot = (w.t0 + t) * kTileKeys + et;  // t0 = 0 in the sparse form
         bool valid = false;
         if (kSparse) {
           if (slot < tl) {
@@ -423,6 +423,26 @@ __device__ __forceinline__ void fused_body(const KernelParams& p, const CUtensor
                 unpack_f32x2(fma_f32x2(xx[k], c2c2, pack_f32x2(nl.x, nl.y)), y0, y1);
                 s01 = add_f32x2(s01, pack_f32x2(fast_exp2(y0), fast_exp2(y1)));
               }
+            }
+          } else if (n == kMaxN) {
+            // 128 heads: a constant trip count, unrolled, so that the loads
+            // and exponentials of neighbouring chunks interleave
+            uint32_t fa[16], ga[16], fb[16], gb[16];
+            tmem_ld16_issue(taddr, fa);
+            tmem_ld16_issue(taddr + kHalfCols, ga);
+            tmem_ld_wait(fa, ga);
+#pragma unroll
+            for (int c0 = 0; c0 < kMaxN; c0 += 32) {
+              tmem_ld16_issue(taddr + c0 + 16, fb);
+              tmem_ld16_issue(taddr + kHalfCols + c0 + 16, gb);
+              l1_16(fa, ga, c0);
+              tmem_ld_wait(fb, gb);
+              if (c0 + 32 < kMaxN) {
+                tmem_ld16_issue(taddr + c0 + 32, fa);
+                tmem_ld16_issue(taddr + kHalfCols + c0 + 32, ga);
+              }
+              l1_16(fb, gb, c0 + 16);
+              if (c0 + 32 < kMaxN) tmem_ld_wait(fa, ga);
             }
           } else {
             uint32_t fa[16], ga[16], fb[16], gb[16];
@@ -532,9 +552,12 @@ __device__ __forceinline__ void fused_body(const KernelParams& p, const CUtensor
         float* o = p.out + static_cast<int64_t>(w.q_tok) * p.topk;
         for (int s = nt * kTileKeys + et; s < p.topk; s += kTileKeys) o[s] = 0.f;
       } else {
+        // to the end of the row, or, for a part of a split pack that is not
+        // the last, to the end of its own key range
+        const int end = w.cut_tail ? min(p.width, (w.t0 + w.ntiles) * kTileKeys) : p.width;
         for (int r = 0; r < w.nrows; ++r) {
           float* o = p.out + static_cast<int64_t>(w.q_tok + r) * p.width;
-          for (int j = nt * kTileKeys + et; j < p.width; j += kTileKeys) o[j] = 0.f;
+          for (int j = (w.t0 + nt) * kTileKeys + et; j < end; j += kTileKeys) o[j] = 0.f;
         }
       }
     }

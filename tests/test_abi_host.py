@@ -149,7 +149,7 @@ def test_compressed_keys_are_accepted_and_bound_the_dense_tiles():
     items, _, info = smla.schedule_host(4, num_heads_q=16, batch_size=1, max_seqlen_q=S1, max_seqlen_k=Sk,
                                         topk=0, mask_mode=3, softmax_scale=0.05, cmp_ratio=c)
     assert info.out_width == Sk
-    for q_tok, nrows, r0, k_base, Sq, Sk_, ntiles, _ in items:
+    for q_tok, nrows, r0, k_base, Sq, Sk_, ntiles, *_ in items:
         last = r0 + nrows - 1
         vis = min(Sk, max(0, last + Sk * c + (c - 1) - S1 + 1) // c)
         assert ntiles == -(-vis // 128)
@@ -199,6 +199,71 @@ def test_topk_length_hint_drives_the_estimate():
 def test_dense_items_respect_causal_visibility():
     items, _, _ = smla.schedule_host(8, num_heads_q=16, batch_size=1, max_seqlen_q=512,
                                      max_seqlen_k=512, topk=0, mask_mode=3, softmax_scale=0.05)
-    for q_tok, nrows, r0, k_base, Sq, Sk, ntiles, _ in items:
+    for q_tok, nrows, r0, k_base, Sq, Sk, ntiles, *_ in items:
         last = r0 + nrows - 1
         assert ntiles == -(-min(512, last + 1) // 128)
+
+
+# ---------------------------------------------------------------- dense key split
+def _split_cover(items, width):
+    """(token pack, key tile) -> count over the items, and the tail writers."""
+    cover, tails = {}, {}
+    for q_tok, nrows, r0, k_base, Sq, Sk, ntiles, b, t0, cut, r1, r2 in items:
+        assert r1 == 0 and r2 == 0 and t0 >= 0 and ntiles >= 0 and cut in (0, 1)
+        for t in range(t0, t0 + ntiles):
+            cover[(q_tok, t)] = cover.get((q_tok, t), 0) + 1
+        if cut == 0:
+            tails[q_tok] = tails.get(q_tok, 0) + 1
+    return cover, tails
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 5])
+@pytest.mark.parametrize("layout", ["BSND", "TND"])
+def test_dense_split_covers_every_key_tile_once(split, layout):
+    """Split into parts of at most ``split`` key tiles, the dense schedule
+    covers each (token pack, key tile) of the whole-pack schedule exactly
+    once, parts of a pack are contiguous from tile 0, and exactly one part of
+    each pack (the last) zeroes the row past its tiles."""
+    if layout == "TND":
+        lens_q, lens_k = [7, 300, 0, 129, 700], [9, 513, 3, 129, 640]
+        kw = dict(layout="TND", cu_seqlens_q=np.concatenate([[0], np.cumsum(lens_q)]).tolist(),
+                  cu_seqlens_k=np.concatenate([[0], np.cumsum(lens_k)]).tolist(), batch_size=5,
+                  max_seqlen_k=max(lens_k))
+    else:
+        kw = dict(layout="BSND", batch_size=2, max_seqlen_q=700, max_seqlen_k=900)
+    for mask in (0, 3):
+        whole, _, _ = smla.schedule_host(37, num_heads_q=16, topk=0, mask_mode=mask, softmax_scale=0.05, **kw)
+        parts, offs, info = smla.schedule_host(37, split_tiles=split, num_heads_q=16, topk=0, mask_mode=mask,
+                                               softmax_scale=0.05, **kw)
+        assert info.split_tiles == split and info.split_items == len(parts) == offs[-1]
+        want = {(it[0], t): 1 for it in whole for t in range(it[6])}
+        cover, tails = _split_cover(parts, info.out_width)
+        assert cover == want
+        assert sorted(tails) == sorted(it[0] for it in whole) and set(tails.values()) == {1}
+        assert all(it[6] <= split for it in parts)
+        # the tail part is the pack's last: no part of the pack starts after it
+        last_t0 = {}
+        for it in parts:
+            last_t0[it[0]] = max(last_t0.get(it[0], 0), it[8])
+        assert all(it[8] == last_t0[it[0]] for it in parts if it[9] == 0)
+
+
+def test_dense_split_choice():
+    """The dense L1-norm launch splits a few long packs (2 x 512 causal
+    tokens of 16 heads: 128 packs of up to 4 tiles for 152 CTAs) and leaves a
+    schedule that is already balanced alone; the sparse form never splits."""
+    _, _, info = smla.schedule_host(152, want_items=False, split_tiles=-1, num_heads_q=16, batch_size=2,
+                                    max_seqlen_q=512, max_seqlen_k=512, topk=0, mask_mode=3, softmax_scale=0.05)
+    assert 0 < info.split_tiles < 4 and info.split_items > 128
+    whole = smla.schedule_host(152, want_items=False, num_heads_q=16, batch_size=2, max_seqlen_q=512,
+                               max_seqlen_k=512, topk=0, mask_mode=3, softmax_scale=0.05)[2]
+    assert info.max_cta_cost < 0.9 * whole.max_cta_cost
+    _, _, info = smla.schedule_host(152, want_items=False, split_tiles=-1, num_heads_q=16, batch_size=8,
+                                    max_seqlen_q=4096, max_seqlen_k=4096, topk=0, mask_mode=0, softmax_scale=0.05)
+    assert info.split_tiles == 0 and info.split_items == 0
+    _, _, info = smla.schedule_host(152, want_items=False, split_tiles=-1, num_heads_q=128, batch_size=1,
+                                    max_seqlen_q=64, max_seqlen_k=4096, topk=2048, mask_mode=3, softmax_scale=0.05)
+    assert info.split_tiles == 0
+    with pytest.raises(smla.SmlaError):
+        smla.schedule_host(152, want_items=False, split_tiles=2, num_heads_q=128, batch_size=1, max_seqlen_q=64,
+                           max_seqlen_k=4096, topk=2048, mask_mode=3, softmax_scale=0.05)

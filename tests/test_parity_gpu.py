@@ -439,3 +439,71 @@ def test_seqused_full_lengths_bitwise_equal_to_run(lib):
                  seqused_q=full, seqused_k=fullk)
     torch.cuda.synchronize()
     assert np.array_equal(a.view(np.uint32), b.cpu().numpy().view(np.uint32))
+
+
+# ---------------------------------------------------------------- dense key split
+@pytest.mark.parametrize("split", [1, 2, 4])
+@pytest.mark.parametrize("mask", [0, 3])
+def test_dense_split_along_keys(lib, monkeypatch, split, mask):
+    """Dense L1-norm launch with each token pack's key tiles split into parts
+    (forced with SMLA_SPLIT; the plan splits by itself only when few long
+    packs would unbalance the grid).  6 key tiles and a ragged tail per
+    pack; parts zero only their own uncomputed range, the last part the rest
+    of the row.  Compared with the oracle, and bit for bit with the unsplit
+    launch: a slot's sum over the heads is computed the same way by
+    whichever CTA owns it."""
+    w = W.make_workload(layout="BSND", dtype="bf16", B=2, S1=50, S2=700, G=16, topk=0, mask_mode=mask,
+                        seed=7300 + split + 10 * mask, lse=None)
+    exact_lse(oracle, w)
+    want = oracle.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **oracle_kwargs(w))
+    t = to_device(w)
+    monkeypatch.setenv("SMLA_SPLIT", str(split))
+    got, plan, _, status = run_gpu(lib, w, tensors=t)
+    assert plan.info.split_tiles == split and plan.info.split_items > plan.info.num_items
+    assert status[0] == lib.SMLA_OK
+    assert_close(got, want, what=f"dense split {split}")
+    rows = got.reshape(w.n_tokens, -1).astype(np.float64)
+    assert np.all(rows[invalid_slot_mask(w)] == 0.0)
+    assert np.all(np.abs(rows.sum(axis=1) - 1.0) <= ROWSUM_TOL)
+    monkeypatch.setenv("SMLA_SPLIT", "0")
+    whole, plan0, _, _ = run_gpu(lib, w, tensors=t)
+    assert plan0.info.split_tiles == 0
+    assert np.array_equal(whole.view(np.uint32), got.view(np.uint32))
+    # the forward LSE launch of a split plan takes whole packs
+    lse = plan.softmax_lse(t["q"], t["k"])
+    torch.cuda.synchronize()
+    l = lse.cpu().numpy().reshape(w.n_tokens, w.G).astype(np.float64)
+    ref = w.lse_rows().astype(np.float64)
+    assert np.all(np.abs(l - ref) <= 1e-4 + 1e-6 * np.abs(ref))
+
+
+def test_dense_split_with_seqused_and_compressed_keys(lib, monkeypatch):
+    """Parts of a split pack under seqused_q / seqused_k (the pack's visible
+    tiles end inside or before a part) and with compressed keys."""
+    monkeypatch.setenv("SMLA_SPLIT", "1")
+    w = W.make_workload(name="split_seqused", layout="TND", dtype="bf16", seqlens_q=[70, 9, 130],
+                        seqlens_k=[400, 9, 300], G=16, topk=0, mask_mode=3, max_seqlen_k=420,
+                        seed=7310, lse=None)
+    seqused_parity(lib, w, su_q=[50, 9, 3], su_k=[1000, 0, 200])
+    w = W.make_workload(name="split_cmp", layout="BSND", dtype="fp16", B=2, S1=300, S2=400, G=16, topk=0,
+                        mask_mode=3, seed=7311, lse=None)
+    res = np.asarray([1, 3], np.int32)
+    okw = dict(oracle_kwargs(w), cmp_ratio=4, cmp_residual_k=res)
+    W.set_lse_rows(w, oracle.softmax_lse(w.q_bits, w.k_bits, **okw).astype(np.float32))
+    want = oracle.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **okw)
+    plan = lib.Plan(**plan_kwargs(w, cmp_ratio=4))
+    assert plan.info.split_tiles == 1
+    t = to_device(w)
+    out = plan.run(t["q"], t["k"], t["lse"], cmp_residual_k=torch.tensor(res, device="cuda"))
+    torch.cuda.synchronize()
+    assert plan.status()[0] == lib.SMLA_OK
+    assert_close(out.cpu().numpy(), want, what="split, compressed keys")
+
+
+def test_config2_plan_splits_by_itself(lib):
+    """The 2 x 512 causal dense workload (128 packs of 1-4 key tiles for 152
+    CTAs) is split by the plan without any override; full parity is the
+    config-2 test above."""
+    w = W.make_config(2)
+    plan = lib.Plan(**plan_kwargs(w))
+    assert plan.info.split_tiles > 0 and plan.info.split_items > plan.info.num_items
