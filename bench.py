@@ -36,7 +36,8 @@ METRIC = "selected q.k pairs/s (Softmax-L1Norm forward, whole job)"
 UNIT = "pairs/s"
 L2_FLUSH_BYTES = 512 << 20   # > the 129 MB L2
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "smla_fused_kernel_dsv32_traffic.txt")
-KERNEL_SRC = os.path.join(ROOT, "softmax_l1_norm_gb300", "csrc", "smla_kernel.cu")
+# the single-CTA kernel and the device code it shares with the CTA-pair kernel
+KERNEL_SRCS = [os.path.join(ROOT, "softmax_l1_norm_gb300", "csrc", f) for f in ("smla_kernel.cu", "smla_device.cuh")]
 
 
 # ----------------------------------------------------------------------------
@@ -100,11 +101,13 @@ def load_peaks():
 
 
 def kernel_sha():
-    """Hash of the kernel source with comments and blank lines removed, so
+    """Hash of the kernel sources with comments and blank lines removed, so
     that edits to comments keep the profiled traffic valid."""
     import re
-    with open(KERNEL_SRC, encoding="utf-8") as f:
-        src = f.read()
+    src = ""
+    for path in KERNEL_SRCS:
+        with open(path, encoding="utf-8") as f:
+            src += f.read() + "\n"
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     src = re.sub(r"//[^\n]*", "", src)
     code = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
