@@ -507,3 +507,46 @@ def test_config2_plan_splits_by_itself(lib):
     w = W.make_config(2)
     plan = lib.Plan(**plan_kwargs(w))
     assert plan.info.split_tiles > 0 and plan.info.split_items > plan.info.num_items
+
+
+# ---------------------------------------------------------------- CTA pairs under cut lengths / compressed keys
+def test_cta_pair_kernel_with_seqused(lib, monkeypatch):
+    """The CTA-pair kernel (forced) under seqused_q / seqused_k: rows past
+    seqused_q are zero, keys past seqused_k masked, the causal diagonal on
+    the cut lengths; against the oracle, and against the single-CTA kernel
+    (within the tolerance: the two kernels split the head dimension
+    between their issuers differently, so fp32 partial sums round apart)."""
+    monkeypatch.setenv("SMLA_PAIR", "1")
+    w = W.make_workload(name="pair_seqused", layout="BSND", dtype="bf16", B=3, S1=30, S2=1500, G=128,
+                        topk=1100, mask_mode=3, seed=7400, lse=None)
+    got = seqused_parity(lib, w, su_q=[30, 11, 0], su_k=[1500, 700, 9])
+    monkeypatch.setenv("SMLA_PAIR", "0")
+    single = seqused_parity(lib, w, su_q=[30, 11, 0], su_k=[1500, 700, 9])
+    assert_close(got, single, what="pair vs single-CTA kernel")
+    assert np.array_equal(got == 0.0, single == 0.0)
+
+
+def test_cta_pair_kernel_with_compressed_keys(lib, monkeypatch):
+    """The CTA-pair kernel (forced) with compressed keys of ratio 4 and
+    per-sequence residuals under the causal mask."""
+    monkeypatch.setenv("SMLA_PAIR", "1")
+    w = W.make_workload(name="pair_cmp", layout="BSND", dtype="bf16", B=2, S1=64, S2=600, G=128, topk=700,
+                        mask_mode=3, seed=7401, lse=None, with_topk_length=False)
+    rng = np.random.Generator(np.random.PCG64(7401))
+    w.sparse_indices = rng.integers(-1, 620, size=w.sparse_indices.shape).astype(np.int32)
+    res = np.asarray([0, 3], np.int32)
+    okw = dict(oracle_kwargs(w), cmp_ratio=4, cmp_residual_k=res)
+    W.set_lse_rows(w, oracle.softmax_lse(w.q_bits, w.k_bits, **okw).astype(np.float32))
+    want = oracle.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **okw)
+    plan = lib.Plan(**plan_kwargs(w, cmp_ratio=4))
+    assert plan.info.cta_pairs > 0
+    t = to_device(w)
+    out = plan.run(t["q"], t["k"], t["lse"], sparse_indices=t["idx"], cmp_residual_k=torch.tensor(res, device="cuda"))
+    torch.cuda.synchronize()
+    assert plan.status()[0] in (lib.SMLA_OK, lib.SMLA_WARN_BAD_INDEX)
+    got = out.cpu().numpy()
+    assert_close(got, want, what="CTA pairs, compressed keys")
+    rows = got.reshape(w.n_tokens, -1).astype(np.float64)
+    assert np.all(rows[want.reshape(w.n_tokens, -1) == 0.0] == 0.0)
+    has = ~np.isneginf(w.lse_rows()[:, 0])
+    assert np.all(np.abs(rows[has].sum(axis=1) - 1.0) <= ROWSUM_TOL)
