@@ -508,18 +508,23 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   }
 
   // CTA pairs for the L1-norm launch (sparse form, N = 128).  The pair
-  // kernel splits each token's tiles between two SMs, so it pays off when
-  // tokens are long: measured on GB300, 0.79 vs 0.72 of the bf16 peak with
-  // 32768 tokens of top-2048 (15.9 tiles a token), but 0.53 vs 0.61 with
-  // 4096 causal tokens (12.3 tiles a token).  It runs when the schedule's
-  // mean is at least kPairMinTiles tiles a token; SMLA_PAIR=0 / 1 forces the
-  // choice.  As many clusters as fit on the device at once.
+  // kernel splits each token's tiles between two SMs and holds twice the key
+  // bytes in flight per SM, which pays off when tokens are long and the key
+  // gather's latency is high.  Measured on GB300 (one box, clustered top-2048
+  // tokens of 15.9 tiles): 8192 tokens and keys 1.52 ms against 1.44 on one
+  // CTA per SM, 16384 2.89 against 2.94, 32768 5.66-5.70 against 5.96; 4096
+  // causal tokens of 12.3 tiles: 0.83 against 0.71 ms.  It runs when the
+  // schedule's mean is at least kPairMinTiles tiles a token and there are at
+  // least kPairMinKeyRows key rows; SMLA_PAIR=0 / 1 forces the choice.  As
+  // many clusters as fit on the device at once.
   constexpr double kPairMinTiles = 14.0;
+  constexpr int64_t kPairMinKeyRows = 16384;
   Schedule ps;
   const char* pair_env = std::getenv("SMLA_PAIR");
   const int pair_force = pair_env == nullptr ? -1 : (std::atoi(pair_env) != 0 ? 1 : 0);
   const double mean_tiles = static_cast<double>(s.est_tiles) / static_cast<double>(std::max<int64_t>(1, g.n_tokens));
-  const bool want_pair = pair_force == 1 || (pair_force == -1 && mean_tiles >= kPairMinTiles);
+  const bool want_pair =
+      pair_force == 1 || (pair_force == -1 && mean_tiles >= kPairMinTiles && g.k_rows >= kPairMinKeyRows);
   if (g.sparse && g.n_mma == 128 && want_pair) {
     int clusters = 0;
     if (smla::configure_pair(optin, &clusters) == cudaSuccess && clusters > 0) {

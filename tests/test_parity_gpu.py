@@ -269,26 +269,34 @@ def test_fused_kernel_waits_give_up_and_report(lib, monkeypatch):
     device waits are bounded by 30 ms: the MMA issuers' wait for that chunk
     runs out, sets the CTA's abort flag and the timeout bit; every role leaves
     its loop, copies and MMAs in flight are drained and TMEM is released.
-    Each launch mode reports SMLA_ERR_TIMEOUT, and afterwards the context
-    still computes the oracle's result with a normal plan."""
+    Each launch mode reports SMLA_ERR_TIMEOUT -- the L1-norm launch on the
+    single-CTA kernel and on the CTA-pair kernel (forced) -- and afterwards
+    the context still computes the oracle's result with a normal plan."""
     w = W.make_workload(layout="BSND", dtype="bf16", B=1, S1=64, S2=2500, G=128, topk=2048, mask_mode=3,
                         seed=5200, lse=None)
     exact_lse(oracle, w)
     t = to_device(w)
     monkeypatch.setenv("SMLA_WAIT_TIMEOUT_MS", "30")
     monkeypatch.setenv("SMLA_DEBUG_WITHHOLD_Q", "1")
+    monkeypatch.setenv("SMLA_PAIR", "0")
     plan0 = lib.Plan(**plan_kwargs(w))
+    monkeypatch.setenv("SMLA_PAIR", "1")
+    plan_pair = lib.Plan(**plan_kwargs(w))
+    monkeypatch.delenv("SMLA_PAIR")
     monkeypatch.delenv("SMLA_WAIT_TIMEOUT_MS")
     monkeypatch.delenv("SMLA_DEBUG_WITHHOLD_Q")
+    assert plan0.info.cta_pairs == 0 and plan_pair.info.cta_pairs > 0
     runs = {
-        "l1": lambda: plan0.run(t["q"], t["k"], t["lse"], sparse_indices=t["idx"], topk_length=t["tl"]),
-        "lse": lambda: plan0.softmax_lse(t["q"], t["k"], sparse_indices=t["idx"], topk_length=t["tl"]),
-        "fused": lambda: plan0.run_fused_lse(t["q"], t["k"], sparse_indices=t["idx"], topk_length=t["tl"]),
+        "l1": (plan0, lambda: plan0.run(t["q"], t["k"], t["lse"], sparse_indices=t["idx"], topk_length=t["tl"])),
+        "l1 pair": (plan_pair, lambda: plan_pair.run(t["q"], t["k"], t["lse"], sparse_indices=t["idx"],
+                                                     topk_length=t["tl"])),
+        "lse": (plan0, lambda: plan0.softmax_lse(t["q"], t["k"], sparse_indices=t["idx"], topk_length=t["tl"])),
+        "fused": (plan0, lambda: plan0.run_fused_lse(t["q"], t["k"], sparse_indices=t["idx"], topk_length=t["tl"])),
     }
-    for name, fn in runs.items():
+    for name, (pl, fn) in runs.items():
         fn()
         torch.cuda.synchronize()
-        code, flags = plan0.status()
+        code, flags = pl.status()
         assert code == lib.SMLA_ERR_TIMEOUT and (flags & 2), (name, code, flags)
     got, plan, _, status = run_gpu(lib, w, tensors=t)
     assert status[0] == lib.SMLA_OK
