@@ -404,7 +404,12 @@ struct smla_plan {
 
 namespace {
 
-constexpr int kHostChunks = 4;
+// run_from_host pipelines over as many token chunks as leave every CTA two
+// work items in each, at most kMaxHostChunks, and only when that is at least
+// kMinHostChunks (else one copy, one kernel, one copy).  Measured on the
+// 4096-token workload: 3.06 ms a step with 4 chunks, 3.00 with 6, 2.98 with 8.
+constexpr int kMinHostChunks = 4;
+constexpr int kMaxHostChunks = 8;
 
 void release_plan(smla_plan* plan) {
   for (cudaEvent_t e : plan->events) cudaEventDestroy(e);
@@ -486,17 +491,19 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   plan->items_host = s.items;
 
   // Token chunks for run_from_host: cut the token-ordered work items into
-  // kHostChunks runs of about equal token count (an item never straddles a
-  // cut), when there is enough work for every CTA in each chunk.
+  // runs of about equal token count (an item never straddles a cut), when
+  // there is enough work for every CTA in each chunk.
   std::vector<Schedule> cs;
-  if (static_cast<int64_t>(s.items.size()) >= static_cast<int64_t>(kHostChunks) * ctas * 2) {
+  const int n_chunks = static_cast<int>(
+      std::min<int64_t>(kMaxHostChunks, static_cast<int64_t>(s.items.size()) / (2 * static_cast<int64_t>(ctas))));
+  if (n_chunks >= kMinHostChunks) {
     std::vector<WorkItem> ordered = s.items;
     std::sort(ordered.begin(), ordered.end(), [](const WorkItem& a, const WorkItem& b) { return a.q_tok < b.q_tok; });
     int64_t cut = 0;
     plan->chunk_lo.push_back(0);
     for (const WorkItem& w : ordered) {
       const int next_chunk = static_cast<int>(plan->chunk_lo.size());
-      if (next_chunk < kHostChunks && w.q_tok >= g.n_tokens * next_chunk / kHostChunks && w.q_tok > cut) {
+      if (next_chunk < n_chunks && w.q_tok >= g.n_tokens * next_chunk / n_chunks && w.q_tok > cut) {
         plan->chunk_hi.push_back(w.q_tok);
         plan->chunk_lo.push_back(w.q_tok);
         cut = w.q_tok;

@@ -178,7 +178,7 @@ def test_run_from_host_pipelined_matches_run(lib, kind):
         w = W.make_workload(layout="TND", dtype="fp16", seqlens_q=[70, 130, 40], seqlens_k=[90, 130, 60],
                             G=64, topk=0, mask_mode=3, seed=2851)
     a, plan, t, _ = run_gpu(lib, w, num_ctas=8)
-    assert plan.info.host_chunks == 4
+    assert plan.info.host_chunks >= 4
     pin = {k: (None if v is None else v.cpu().pin_memory()) for k, v in
            {"q": t["q"], "k": t["k"], "lse": t["lse"], "indices": t["idx"], "topk_length": t["tl"]}.items()}
     pin["out"] = torch.full(plan.output_shape, float("nan"), dtype=torch.float32).pin_memory()
