@@ -110,7 +110,8 @@ typedef enum { SMLA_MASK_NONE = 0, SMLA_MASK_RIGHT_DOWN_CAUSAL = 3 } smla_mask_m
  *                       expected topk_length, used only to balance the work
  *                       schedule.  NULL = estimate min(topk, visible keys).
  *   num_ctas            0 = one persistent CTA per SM of the current device;
- *                       > 0 forces a grid size (tests, multi-tenant use).
+ *                       > 0 forces a grid size (tests, multi-tenant use); the
+ *                       CTA-pair launch then runs at most num_ctas / 2 pairs.
  */
 typedef struct {
   int32_t layout_q;

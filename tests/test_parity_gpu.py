@@ -262,6 +262,11 @@ def test_cta_pair_kernel(lib, monkeypatch, topk, S2, mask):
     assert_close(single, want, what="single-CTA kernel")
     again, _, _, _ = run_gpu(lib, w, plan=plan, tensors=t)
     assert np.array_equal(again.view(np.uint32), got.view(np.uint32)), "pair kernel run to run"
+    # a grid size the caller asks for bounds the pairs too; the bits do not change
+    monkeypatch.setenv("SMLA_PAIR", "1")
+    small, plan7, _, _ = run_gpu(lib, w, tensors=t, num_ctas=7)
+    assert plan7.info.cta_pairs == 3
+    assert np.array_equal(small.view(np.uint32), got.view(np.uint32)), "pair kernel on 3 clusters"
 
 
 def test_fused_kernel_waits_give_up_and_report(lib, monkeypatch):
