@@ -440,7 +440,7 @@ def make_plan(smla, w):
                      cu_seqlens_k=None if w.cu_seqlens_k is None else w.cu_seqlens_k.tolist())
 
 
-def other_config_line(smla, n, steps, device, stream, flush):
+def other_config_line(smla, n, steps, device, stream, flush, gpu_id=None):
     """One configuration other than the headline, timed the same way (after
     the headline's timed region): median ms per launch and the roofline."""
     import torch
@@ -457,7 +457,10 @@ def other_config_line(smla, n, steps, device, stream, flush):
     for _ in range(3):
         flush()
         fn()
-    times = timed_launches(fn, steps, stream, flush)
+    torch.cuda.synchronize(device)
+    with ClockSampler(gpu_id if gpu_id is not None else device.index) as clocks:
+        time.sleep(0.3)  # the sampler's first readings
+        times = timed_launches(fn, steps, stream, flush)
     code, flags = plan.status(stream)
     if code != smla.SMLA_OK:
         raise RuntimeError(f"config {n}: device status {code} flags {flags}")
@@ -467,6 +470,7 @@ def other_config_line(smla, n, steps, device, stream, flush):
     line = {"workload": w.name, "ms_per_launch": st, "pairs_per_s": pairs / sec, "tflops": flops / sec / 1e12,
             "pairs": pairs, "flops": flops, "roofline": roofline_block(flops, sum(compulsory.values()), sec,
                                                                       hbm_gbs, bf16_tf, src),
+            "clocks": clocks.summary(),
             "north_star_roofline": north_star_block(sum(bytes_.values()), sec, hbm_gbs,
                                                     flops / (bf16_tf * 1e12)),
             "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "num_items", "stages",
@@ -623,7 +627,8 @@ def run_ours(args, world, rank, local):
         others = {}
         for n in (1, 2, 3, 4, 5):
             if n != args.config:
-                others[str(n)] = other_config_line(smla, n, args.other_steps, device, stream, flush)
+                others[str(n)] = other_config_line(smla, n, args.other_steps, device, stream, flush,
+                                                   gpu_uuid if gpu_uuid else local)
 
     if rank != 0:
         return 0
