@@ -399,8 +399,8 @@ smla_status smla_debug_wait_timeout_probe(int64_t timeout_ns, smla_stream_t stre
  *
  * A slot whose key position j is in [0, Sk) holds key row j of the token's
  * sequence, bit for bit; any other slot (index -1 or out of range, slot
- * past topk_length or topk) holds the sequence's key 0, which the epilogue
- * masks to an output of 0.  Asynchronous on ``stream``; device flags go to
+ * past topk_length or topk) holds zeros (nothing is read for it), and the
+ * epilogue masks it to an output of 0.  Asynchronous on ``stream``; device flags go to
  * the plan's status word.  Returns SMLA_ERR_INVALID for a bad mode, token or
  * alignment, SMLA_ERR_NULLPTR for a missing pointer.
  */

@@ -161,9 +161,10 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
-// 16 bytes global -> shared, cached in L2 only.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// 16 bytes global -> shared, cached in L2 only; with `copy` false nothing
+// is read and the 16 bytes are zero-filled (src must still be a valid address).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool copy = true) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(copy ? 16 : 0) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
@@ -633,8 +634,11 @@ __device__ __forceinline__ void produce_keys(const KernelParams& p, int pw, int 
   if (have) fetch_indices(cur);
   const uint8_t* kseg = p.k + seg * 16;
   while (have && ok) {
-    // source key rows of this tile (invalid slots read key 0 of the sequence)
+    // source key rows of this tile; an invalid slot (index -1 or out of
+    // range, past topk_length or topk, past the keys) is zero-filled without
+    // a read (its address is kept valid: key 0 of the sequence)
     int64_t row[kKeysPerLane];
+    uint32_t inmask = 0;
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < kKeysPerLane; ++i) {
@@ -642,6 +646,7 @@ __device__ __forceinline__ void produce_keys(const KernelParams& p, int pw, int 
       const bool in = (j >= 0) && (j < cur.w.Sk);
       if (kSparse) bad |= (krow0 + 4 * i + cursor_ktile<kPair>(cur) * kTileKeys < cur.tl) && !in && (j != -1);
       row[i] = static_cast<int64_t>(cur.w.k_base) + (in ? j : 0);
+      inmask |= (in ? 1u : 0u) << i;
     }
     if (kSparse && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kFlagBadIndex);
     TileCursor nxt = cur;
@@ -657,7 +662,7 @@ __device__ __forceinline__ void produce_keys(const KernelParams& p, int pw, int 
 #pragma unroll
       for (int i = 0; i < kKeysPerLane; ++i) {
         const int r = krow0 + 4 * i;
-        cp_async_16(dst + r * 128 + ((seg ^ (r & 7)) << 4), kc + row[i] * (kHeadDim * 2));
+        cp_async_16(dst + r * 128 + ((seg ^ (r & 7)) << 4), kc + row[i] * (kHeadDim * 2), (inmask >> i) & 1u);
       }
       cp_async_arrive_noinc(bar_k_full + 8 * kst);
       kst += kWide ? 1u : kStep;

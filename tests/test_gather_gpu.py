@@ -7,8 +7,8 @@ that copies every shared-memory ring stage out exactly as the MMA reads it.
 Each stage is compared byte for byte with the key rows the slots name,
 placed by the definition of the 128-byte swizzle (16-byte piece p of row s
 of an 8-row group at position p XOR (s mod 8)).  Invalid slots (index -1,
-out of range, past topk_length or topk) must hold key 0 of the row's
-sequence: the epilogue masks them, and the gather reads a row that exists.
+out of range, past topk_length or topk, past the sequence's keys) must hold
+zeros: nothing is read for them, and the epilogue masks them.
 """
 import numpy as np
 import pytest
@@ -52,8 +52,10 @@ def expected_stages(w, token, R):
         vis = Sk if w.mask_mode == 0 else min(Sk, max(0, last + Sk - Sq + 1))
         ntiles = -(-min(vis, w.out_width) // 128)
         j = np.arange(ntiles * 128)
-    rows = k0 + np.where((j >= 0) & (j < Sk), j, 0)
-    src = keys[rows].reshape(ntiles, 128, 8, 8, 16).transpose(0, 2, 1, 3, 4)  # tile, chunk, slot, piece, byte
+    valid = (j >= 0) & (j < Sk)
+    gathered = keys[k0 + np.where(valid, j, 0)].copy()
+    gathered[~valid] = 0   # invalid slots are zero-filled
+    src = gathered.reshape(ntiles, 128, 8, 8, 16).transpose(0, 2, 1, 3, 4)  # tile, chunk, slot, piece, byte
     # position q of slot s holds piece q XOR (s mod 8)
     piece_at = np.arange(8)[None, :] ^ (np.arange(128)[:, None] & 7)
     out = np.take_along_axis(src, piece_at[None, None, :, :, None], axis=3)
@@ -91,7 +93,7 @@ def test_gather_sparse_padding_and_ragged_tail(lib):
 
 def test_gather_out_of_range_indices_without_topk_length(lib):
     """No topk_length: every slot is a candidate; indices below -1 or past Sk
-    read key 0 (and raise the bad-index flag)."""
+    give zero rows (and raise the bad-index flag)."""
     w = W.make_workload(layout="BSND", dtype="fp16", B=2, S1=6, S2=300, G=16, topk=200, mask_mode=0,
                         seed=5101, with_topk_length=False)
     rng = np.random.Generator(np.random.PCG64(5101))
