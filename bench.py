@@ -35,9 +35,15 @@ import workloads as W  # noqa: E402
 METRIC = "selected q.k pairs/s (Softmax-L1Norm forward, whole job)"
 UNIT = "pairs/s"
 L2_FLUSH_BYTES = 512 << 20   # > the 129 MB L2
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "smla_fused_kernel_dsv32_traffic.txt")
-# the single-CTA kernel and the device code it shares with the CTA-pair kernel
-KERNEL_SRCS = [os.path.join(ROOT, "softmax_l1_norm_gb300", "csrc", f) for f in ("smla_kernel.cu", "smla_device.cuh")]
+# Per L1-norm kernel: its ncu DRAM-traffic summary and the sources it is
+# built from (its own file and the device code the two kernels share).
+_CSRC = os.path.join(ROOT, "softmax_l1_norm_gb300", "csrc")
+KERNELS = {
+    "smla_fused_kernel": (os.path.join(ROOT, "profiles", "smla_fused_kernel_dsv32_traffic.txt"),
+                          [os.path.join(_CSRC, f) for f in ("smla_kernel.cu", "smla_device.cuh")]),
+    "smla_pair_kernel": (os.path.join(ROOT, "profiles", "smla_pair_kernel_dsv32_traffic.txt"),
+                         [os.path.join(_CSRC, f) for f in ("smla_pair.cu", "smla_device.cuh")]),
+}
 
 
 # ----------------------------------------------------------------------------
@@ -100,12 +106,17 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def kernel_sha():
-    """Hash of the kernel sources with comments and blank lines removed, so
+def l1_kernel_name(plan):
+    """The kernel a plan's L1-norm launch runs."""
+    return "smla_pair_kernel" if plan.info.cta_pairs > 0 else "smla_fused_kernel"
+
+
+def kernel_sha(kernel="smla_fused_kernel"):
+    """Hash of a kernel's sources with comments and blank lines removed, so
     that edits to comments keep the profiled traffic valid."""
     import re
     src = ""
-    for path in KERNEL_SRCS:
+    for path in KERNELS[kernel][1]:
         with open(path, encoding="utf-8") as f:
             src += f.read() + "\n"
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
@@ -114,18 +125,20 @@ def kernel_sha():
     return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
-def profiled_traffic(config_name):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
-    if not os.path.exists(PROFILE_TRAFFIC):
+def profiled_traffic(config_name, kernel="smla_fused_kernel"):
+    """DRAM bytes per launch of `kernel` from its committed ncu summary, if
+    that was taken on the current source of the kernel and on this
+    workload; else None."""
+    path = KERNELS[kernel][0]
+    if not os.path.exists(path):
         return None
     kv = {}
-    with open(PROFILE_TRAFFIC) as f:
+    with open(path) as f:
         for line in f:
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-    if kv.get("kernel_sha256_16") != kernel_sha() or kv.get("workload") != config_name:
+    if kv.get("kernel_sha256_16") != kernel_sha(kernel) or kv.get("workload") != config_name:
         return None
     try:
         return float(kv["dram_bytes_per_launch"])
@@ -643,7 +656,8 @@ def run_ours(args, world, rank, local):
                "sample": f"{n_rows} random rows of {name} in {c_secs:.1f}s (fp64 numpy, BLAS threads={threads})"}
 
     per_launch_s = kernel_s / args.steps
-    traffic = profiled_traffic(name)
+    l1_kernel = l1_kernel_name(plan)
+    traffic = profiled_traffic(name, l1_kernel)
     t_tc = flops / (bf16_tf * 1e12)
     line = {
         "metric": METRIC, "value": world * pairs * args.steps / max_s, "unit": UNIT, "n_gpus": world,
@@ -662,7 +676,8 @@ def run_ours(args, world, rank, local):
                    "l2": "flushed before every timed launch: 512 MB written, then 256 MB read (write-backs "
                          "of the flush land before the launch)"},
         "tflops": world * flops * args.steps / max_s / 1e12,
-        "roofline": roofline_block(flops, comp_bytes, per_launch_s, hbm_gbs, bf16_tf, src, traffic),
+        "roofline": dict(roofline_block(flops, comp_bytes, per_launch_s, hbm_gbs, bf16_tf, src, traffic),
+                         kernel=l1_kernel),
         "roofline_tensor": {"achieved": flops / per_launch_s / 1e12, "peak": bf16_tf, "unit": "TFLOP/s",
                             "frac": flops / per_launch_s / 1e12 / bf16_tf, "peak_source": src},
         "north_star_roofline": north_star_block(alg_bytes, per_launch_s, hbm_gbs, t_tc),

@@ -515,23 +515,21 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   }
 
   // CTA pairs for the L1-norm launch (sparse form, N = 128).  The pair
-  // kernel splits each token's tiles between two SMs and holds twice the key
-  // bytes in flight per SM, which pays off when tokens are long and the key
-  // gather's latency is high.  Measured on GB300 (one box, clustered top-2048
-  // tokens of 15.9 tiles): 8192 tokens and keys 1.52 ms against 1.44 on one
-  // CTA per SM, 16384 2.89 against 2.94, 32768 5.66-5.70 against 5.96; 4096
-  // causal tokens of 12.3 tiles: 0.83 against 0.71 ms.  It runs when the
-  // schedule's mean is at least kPairMinTiles tiles a token and there are at
-  // least kPairMinKeyRows key rows; SMLA_PAIR=0 / 1 forces the choice.  As
-  // many clusters as fit on the device at once.
-  constexpr double kPairMinTiles = 14.0;
-  constexpr int64_t kPairMinKeyRows = 16384;
+  // kernel splits each token's tiles between two SMs; one MMA covers both
+  // CTAs' keys and each SM holds 160 KB of keys in flight instead of 96 KB.
+  // Measured on GB300 (one box, pair / single-CTA time, uniform causal and
+  // clustered top-2048 selections): tokens of 4.5 tiles on average 1.06,
+  // 8.5 tiles 0.99-1.01, 12.3 tiles 0.92, 14.1-15.5 tiles 0.88-0.91, from
+  // 4096 to 32768 keys alike.  It runs when the schedule's mean is at least
+  // kPairMinTiles tiles a token; SMLA_PAIR=0 / 1 forces the choice.  As many
+  // clusters as fit on the device at once.
+  constexpr double kPairMinTiles = 10.0;
   Schedule ps;
   const char* pair_env = std::getenv("SMLA_PAIR");
   const int pair_force = pair_env == nullptr ? -1 : (std::atoi(pair_env) != 0 ? 1 : 0);
   const double mean_tiles = static_cast<double>(s.est_tiles) / static_cast<double>(std::max<int64_t>(1, g.n_tokens));
   const bool want_pair =
-      pair_force == 1 || (pair_force == -1 && mean_tiles >= kPairMinTiles && g.k_rows >= kPairMinKeyRows);
+      pair_force == 1 || (pair_force == -1 && mean_tiles >= kPairMinTiles);
   if (g.sparse && g.n_mma == 128 && want_pair) {
     int clusters = 0;
     if (smla::configure_pair(optin, &clusters) == cudaSuccess && clusters > 0) {

@@ -120,7 +120,7 @@ __device__ __forceinline__ void pair_mma_issue(const KernelParams& p, uint32_t s
   const uint32_t S = static_cast<uint32_t>(p.stages);
   const uint32_t idesc = static_cast<uint32_t>(p.idesc);
   uint32_t kst = H, kph = 0, qit = 0, acc = 0;
-  bool ok = true, ready = false, covered = false, acc_ready = false;
+  bool ok = true, ready = false, acc_ready = false;
   WorkItem w_next = it0 < it1 ? p.items[it0] : WorkItem{};
   for (int it = it0; it < it1 && ok; ++it) {
     const WorkItem w = w_next;
@@ -160,9 +160,10 @@ __device__ __forceinline__ void pair_mma_issue(const KernelParams& p, uint32_t s
         if (ws + 2 >= kNumChunks / 2)
           acc_ready = mbar_test_wait_cluster(b.acc_empty + 8 * (buf ^ 1u), (((acc + 1) / kAccBufs) & 1u) ^ 1u);
         // this CTA's producers wrote with cp.async (generic proxy); the peer's
-        // relay fenced its own CTA's stage before forwarding the arrival
-        if (!covered) fence_proxy_async();
-        covered = ready_next;
+        // relay fenced its own CTA's stage before forwarding the arrival.
+        // Fenced for every stage: skipping the fence for a stage acquired
+        // before the previous fence measured no faster.
+        fence_proxy_async();
         tc_fence_after();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {

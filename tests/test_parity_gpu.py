@@ -249,7 +249,7 @@ def test_cta_pair_kernel(lib, monkeypatch, topk, S2, mask):
     exact_lse(oracle, w)
     want = oracle.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **oracle_kwargs(w))
     t = to_device(w)
-    monkeypatch.setenv("SMLA_PAIR", "1")   # these tokens are short: the plan would pick one CTA
+    monkeypatch.setenv("SMLA_PAIR", "1")   # forced: the plan picks one CTA for the short tokens
     got, plan, _, status = run_gpu(lib, w, tensors=t)
     assert plan.info.cta_pairs > 0 and status[0] == lib.SMLA_OK
     assert_close(got, want, what="CTA pair kernel")
@@ -355,20 +355,21 @@ def test_config3_dsv32_full_size_every_row(lib, tmp_path, monkeypatch):
     benchmark's launch configuration: the exact forward LSE is planted on
     every row and every one of the 8.4 M output elements is compared with the
     oracle; every row sums to 1 within 1e-3 and masked slots are exactly 0.
-    Then the same with the CTA-pair kernel forced (the plan picks the
-    single-CTA kernel for this workload)."""
+    The plan picks the CTA-pair kernel for this workload (12.3 key tiles a
+    token); then the same with the single-CTA kernel forced."""
     import oracle_pool
     w = W.make_config(3)
     n_tok = w.n_tokens
     lse, want = oracle_pool.lse_and_rows(w, range(n_tok), str(tmp_path / "c3"))
     W.set_lse_rows(w, lse)
-    got, plan, t, status = run_gpu(lib, w)
-    assert status[0] == lib.SMLA_OK and plan.info.num_ctas == torch.cuda.get_device_properties(0).multi_processor_count
-    assert plan.info.cta_pairs == 0
-    monkeypatch.setenv("SMLA_PAIR", "1")
-    got_pair, plan_pair, _, status = run_gpu(lib, w, tensors=t)
+    monkeypatch.delenv("SMLA_PAIR", raising=False)
+    got_pair, plan_pair, t, status = run_gpu(lib, w)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     assert status[0] == lib.SMLA_OK and plan_pair.info.cta_pairs > 0
-    for name, g in (("single-CTA", got), ("CTA-pair", got_pair)):
+    monkeypatch.setenv("SMLA_PAIR", "0")
+    got, plan, _, status = run_gpu(lib, w, tensors=t)
+    assert status[0] == lib.SMLA_OK and plan.info.cta_pairs == 0 and plan.info.num_ctas == n_sm
+    for name, g in (("CTA-pair", got_pair), ("single-CTA", got)):
         got_rows = g.reshape(n_tok, -1)
         assert_close(got_rows, want, what=f"config 3, every element, {name} kernel")
         sums = got_rows.astype(np.float64).sum(axis=1)
