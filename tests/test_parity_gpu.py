@@ -564,3 +564,50 @@ def test_cta_pair_kernel_with_compressed_keys(lib, monkeypatch):
     assert np.all(rows[want.reshape(w.n_tokens, -1) == 0.0] == 0.0)
     has = ~np.isneginf(w.lse_rows()[:, 0])
     assert np.all(np.abs(rows[has].sum(axis=1) - 1.0) <= ROWSUM_TOL)
+
+
+def pair_and_single(lib, monkeypatch, w):
+    """Oracle parity of the CTA-pair kernel (forced) and of the single-CTA
+    kernel (forced) on the same inputs; returns both outputs and statuses."""
+    exact_lse(oracle, w)
+    want = oracle.softmax_l1_norm(w.q_bits, w.k_bits, w.softmax_lse, **oracle_kwargs(w))
+    t = to_device(w)
+    bad = invalid_slot_mask(w)
+    has = ~np.isneginf(w.lse_rows()[:, 0])
+    res = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("SMLA_PAIR", mode)
+        got, plan, _, status = run_gpu(lib, w, tensors=t)
+        assert (plan.info.cta_pairs > 0) == (mode == "1")
+        name = "CTA-pair" if mode == "1" else "single-CTA"
+        assert_close(got, want, what=f"{w.name}, {name} kernel")
+        rows = got.reshape(w.n_tokens, -1).astype(np.float64)
+        assert np.all(rows[bad] == 0.0), name
+        assert np.all(np.abs(rows[has].sum(axis=1) - 1.0) <= ROWSUM_TOL), name
+        res[mode] = (got, status)
+    return res
+
+
+def test_cta_pair_kernel_tnd_varlen(lib, monkeypatch):
+    """TND layout with 128 heads, queries shorter than their keys (the
+    right-down causal diagonal lets early queries see long prefixes), one
+    sequence with a single query and one with none: the CTA-pair kernel
+    against the oracle and against the single-CTA kernel."""
+    w = W.make_workload(name="pair_tnd", layout="TND", dtype="fp16", seqlens_q=[300, 1, 0, 260, 90],
+                        seqlens_k=[1500, 5, 3, 2100, 1300], G=128, topk=1536, mask_mode=3, seed=7402, lse=None)
+    res = pair_and_single(lib, monkeypatch, w)
+    assert res["1"][1][0] == lib.SMLA_OK and res["0"][1][0] == lib.SMLA_OK
+    assert np.array_equal(res["1"][0] == 0.0, res["0"][0] == 0.0)
+
+
+def test_cta_pair_kernel_without_topk_length_bad_indices(lib, monkeypatch):
+    """No topk_length: all 2048 slots are candidates, with -1 padding and
+    out-of-range indices spread through them (masked and reported by both
+    kernels)."""
+    w = W.make_workload(name="pair_bad_idx", layout="BSND", dtype="bf16", B=2, S1=24, S2=2200, G=128, topk=2048,
+                        mask_mode=3, seed=7403, lse=None, with_topk_length=False)
+    rng = np.random.Generator(np.random.PCG64(7403))
+    w.sparse_indices = rng.integers(-3, 2300, size=w.sparse_indices.shape).astype(np.int32)
+    res = pair_and_single(lib, monkeypatch, w)
+    for mode in ("1", "0"):
+        assert res[mode][1][0] == lib.SMLA_WARN_BAD_INDEX and (res[mode][1][1] & 1)
