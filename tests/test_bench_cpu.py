@@ -107,3 +107,29 @@ def test_workload_numbers_dense_unique_keys():
     pairs, flops, b, comp = bench.workload_numbers(w)
     assert pairs == 2 * (512 * 513 // 2) * 16
     assert comp["k_unique"] == 2 * 512 * 1024 and comp["out"] == 2 * 512 * 512 * 4
+
+
+def test_profiled_traffic_follows_the_kernel_and_its_source(tmp_path, monkeypatch):
+    """The roofline's DRAM traffic is read from the summary of the kernel the
+    L1-norm launch ran, and only while that summary was taken on the
+    kernel's current source and on the same workload."""
+    import bench
+
+    class Info:
+        def __init__(self, pairs):
+            self.info = type("I", (), {"cta_pairs": pairs})()
+
+    assert bench.l1_kernel_name(Info(76)) == "smla_pair_kernel"
+    assert bench.l1_kernel_name(Info(0)) == "smla_fused_kernel"
+    for kernel, (path, srcs) in bench.KERNELS.items():
+        assert all(os.path.exists(s) for s in srcs), kernel
+        summary = tmp_path / f"{kernel}.txt"
+        monkeypatch.setitem(bench.KERNELS, kernel, (str(summary), srcs))
+        body = "# comment: not a field\nworkload: wl\nkernel_sha256_16: {}\ndram_bytes_per_launch: 1234\n"
+        summary.write_text(body.format(bench.kernel_sha(kernel)))
+        assert bench.profiled_traffic("wl", kernel) == 1234.0
+        assert bench.profiled_traffic("other", kernel) is None
+        summary.write_text(body.format("0" * 16))
+        assert bench.profiled_traffic("wl", kernel) is None
+    # the two kernels hash different sources
+    assert bench.kernel_sha("smla_pair_kernel") != bench.kernel_sha("smla_fused_kernel")
