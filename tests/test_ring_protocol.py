@@ -29,9 +29,11 @@ import random
 import pytest
 
 
-def simulate(S, groups, tiles, seed, stall_prob=0.08, issuers=2):
+def simulate(S, groups, tiles, seed, stall_prob=0.08, issuers=2, wide=False):
     """Run the ring protocol once; return (violations, stages consumed).
-    Issuer h takes the stages n with n % issuers == h."""
+    Issuer h takes the stages n with n % issuers == h.  With ``wide`` every
+    group fills its part of every stage, in order (the CTA-pair kernel's
+    32 KB stages): a slot's full phase completes when all groups landed."""
     rng = random.Random(seed)
     N = 8 * tiles
     full = [0] * S    # completed phases of each slot's full barrier
@@ -53,7 +55,8 @@ def simulate(S, groups, tiles, seed, stall_prob=0.08, issuers=2):
     def passes(count, parity):
         return (count & 1) != parity
 
-    prod_next = {g: g for g in range(groups)}      # next stage of each producer group
+    prod_next = {g: (0 if wide else g) for g in range(groups)}  # next stage of each producer group
+    arrivals = [[] for _ in range(S)]  # wide: stages of the groups that landed in the open phase
     iss_next = {h: h for h in range(issuers)}      # next stage of each issuer
     iss_ready = {h: False for h in range(issuers)}  # next stage already acquired by a test
     pipe_free = [0.0]
@@ -81,8 +84,18 @@ def simulate(S, groups, tiles, seed, stall_prob=0.08, issuers=2):
                 push(t + 20.0, "prod", who)
         elif kind == "landed":
             g, n = who
-            full[n % S] += 1
-            prod_next[g] = n + groups
+            if wide:
+                a = arrivals[n % S]
+                if a and a[0] != n:
+                    violations.append(("mixed phase", n, a[0], n))
+                a.append(n)
+                if len(a) == groups:
+                    full[n % S] += 1
+                    a.clear()
+                prod_next[g] = n + 1
+            else:
+                full[n % S] += 1
+                prod_next[g] = n + groups
             push(t + 5.0, "prod", g)   # the group moves on once its copies have landed
         elif kind == "iss":
             n = iss_next[who]
@@ -183,3 +196,17 @@ def test_four_issuers_and_four_groups_need_a_depth_multiple_of_four():
     for seed in range(20):
         violations, consumed = simulate(8, 4, tiles=30, seed=12500 + seed, stall_prob=0.3, issuers=4)
         assert violations == [] and consumed == 240
+
+
+@pytest.mark.parametrize("S", [2, 3, 4, 5, 6, 7])
+def test_wide_stages_filled_by_every_group_in_order_are_safe_at_any_depth(S):
+    """The CTA-pair kernel's ring: each 32 KB stage is filled by both producer
+    groups (one half each), every group in stage order, and two issuers take
+    alternate stages.  A stage is full only once every group landed it, and
+    each group lands its stages in order, so when an issuer's previous stage
+    is full so is every earlier one: no barrier is two phases behind, odd
+    depths included (the kernel runs five)."""
+    for seed in range(20):
+        violations, consumed = simulate(S, 2, tiles=30, seed=13000 + 10 * S + seed, stall_prob=0.3, wide=True)
+        assert violations == [], (S, seed, violations[:3])
+        assert consumed == 240
