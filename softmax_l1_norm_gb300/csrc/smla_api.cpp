@@ -521,8 +521,9 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   // clustered top-2048 selections): tokens of 4.5 tiles on average 1.06,
   // 8.5 tiles 0.99-1.01, 12.3 tiles 0.92, 14.1-15.5 tiles 0.88-0.91, from
   // 4096 to 32768 keys alike.  It runs when the schedule's mean is at least
-  // kPairMinTiles tiles a token; SMLA_PAIR=0 / 1 forces the choice.  As many
-  // clusters as fit on the device at once.
+  // kPairMinTiles tiles a token; SMLA_PAIR=0 / 1 forces the choice for
+  // sparse work with exactly 128 heads.  As many clusters as fit on the
+  // device at once.
   constexpr double kPairMinTiles = 10.0;
   Schedule ps;
   const char* pair_env = std::getenv("SMLA_PAIR");
@@ -530,7 +531,9 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   const double mean_tiles = static_cast<double>(s.est_tiles) / static_cast<double>(std::max<int64_t>(1, g.n_tokens));
   const bool want_pair =
       pair_force == 1 || (pair_force == -1 && mean_tiles >= kPairMinTiles);
-  if (g.sparse && g.n_mma == 128 && want_pair) {
+  // The pair kernel splits q into two 64-head halves and reads 128 LSE
+  // entries a token: exactly 128 heads (N = 128 with no padded columns).
+  if (g.sparse && g.G == 128 && g.n_mma == 128 && want_pair) {
     int clusters = 0;
     if (smla::configure_pair(optin, &clusters) == cudaSuccess && clusters > 0) {
       // a grid size the caller asked for holds for this launch too

@@ -611,3 +611,20 @@ def test_cta_pair_kernel_without_topk_length_bad_indices(lib, monkeypatch):
     res = pair_and_single(lib, monkeypatch, w)
     for mode in ("1", "0"):
         assert res[mode][1][0] == lib.SMLA_WARN_BAD_INDEX and (res[mode][1][1] & 1)
+
+
+@pytest.mark.parametrize("G", [113, 120, 127])
+def test_cta_pairs_only_for_exactly_128_heads(lib, monkeypatch, G):
+    """Head counts of 113-127 pad the MMA's N to 128 as well, but the CTA-pair
+    kernel splits q into two 64-head halves and reads 128 LSE entries a
+    token: the plan keeps such work on one CTA per SM, even when pairs are
+    forced, and the result matches the oracle."""
+    w = W.make_workload(name=f"g{G}_long", layout="BSND", dtype="bf16", B=1, S1=12, S2=2100, G=G, topk=2048,
+                        mask_mode=3, seed=7500 + G, lse=None)
+    for mode in (None, "1"):
+        if mode is None:
+            monkeypatch.delenv("SMLA_PAIR", raising=False)
+        else:
+            monkeypatch.setenv("SMLA_PAIR", mode)
+        got, plan, status = full_parity(lib, w)
+        assert plan.info.cta_pairs == 0 and status[0] == lib.SMLA_OK
