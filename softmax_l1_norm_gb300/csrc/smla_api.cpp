@@ -536,9 +536,14 @@ smla_status smla_l1norm_plan_create(const smla_l1norm_desc* desc, smla_plan** pl
   if (g.sparse && g.G == 128 && g.n_mma == 128 && want_pair) {
     int clusters = 0;
     if (smla::configure_pair(optin, &clusters) == cudaSuccess && clusters > 0) {
-      // a grid size the caller asked for holds for this launch too
-      if (desc->num_ctas > 0) clusters = std::min(clusters, std::max(1, desc->num_ctas / 2));
-      clusters = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(clusters, std::max<int64_t>(1, g.n_tokens))));
+      // a grid size the caller asked for holds for this launch too (one
+      // CTA asked for: no pair)
+      if (desc->num_ctas > 0) clusters = std::min(clusters, desc->num_ctas / 2);
+      clusters = static_cast<int>(std::min<int64_t>(clusters, std::max<int64_t>(1, g.n_tokens)));
+    } else {
+      clusters = 0;
+    }
+    if (clusters > 0) {
       plan->pair_clusters = clusters;
       plan->pair_stages = smla::pair_stages(optin);
       plan->pair_smem = smla::pair_smem_bytes(plan->pair_stages);

@@ -267,6 +267,10 @@ def test_cta_pair_kernel(lib, monkeypatch, topk, S2, mask):
     small, plan7, _, _ = run_gpu(lib, w, tensors=t, num_ctas=7)
     assert plan7.info.cta_pairs == 3
     assert np.array_equal(small.view(np.uint32), got.view(np.uint32)), "pair kernel on 3 clusters"
+    # one CTA asked for: no pair, and the single-CTA kernel's bits on one SM
+    one, plan1c, _, _ = run_gpu(lib, w, tensors=t, num_ctas=1)
+    assert plan1c.info.cta_pairs == 0 and plan1c.info.num_ctas == 1
+    assert np.array_equal(one.view(np.uint32), single.view(np.uint32)), "single-CTA kernel on one CTA"
 
 
 def test_fused_kernel_waits_give_up_and_report(lib, monkeypatch):
