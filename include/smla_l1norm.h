@@ -185,6 +185,15 @@ typedef struct {
  * Test hook: with SMLA_DEBUG_WITHHOLD_Q=1 in the environment at plan
  * creation, every CTA of the plan's launches skips the load of the first q
  * chunk of its first work item, so a wait runs out on purpose.
+ *
+ * Kernel choice for the L1-norm launch (reported in smla_plan_info):
+ * sparse work with exactly 128 heads whose tokens average at least 10
+ * 128-key tiles runs on 2-CTA clusters (cta_pairs > 0), everything else on
+ * one CTA per SM; a dense plan may split token packs along their keys
+ * (split_tiles > 0).  SMLA_PAIR=0 / 1 and SMLA_SPLIT=n in the environment
+ * at plan creation force these choices (SMLA_PAIR=1 still needs exactly
+ * 128 heads and a grid of at least two CTAs).  Every choice computes the
+ * same values to within fp32 rounding.
  */
 smla_status smla_l1norm_plan_create(const smla_l1norm_desc *desc, smla_plan **plan_out);
 
