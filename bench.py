@@ -481,11 +481,12 @@ def other_config_line(smla, n, steps, device, stream, flush, gpu_id=None):
     hbm_gbs, bf16_tf, src = load_peaks()
     sec = st["median"] / 1000.0
     line = {"workload": w.name, "ms_per_launch": st, "pairs_per_s": pairs / sec, "tflops": flops / sec / 1e12,
-            "pairs": pairs, "flops": flops, "roofline": roofline_block(flops, sum(compulsory.values()), sec,
-                                                                      hbm_gbs, bf16_tf, src),
+            "pairs": pairs, "flops": flops,
+            "roofline": dict(roofline_block(flops, sum(compulsory.values()), sec, hbm_gbs, bf16_tf, src),
+                             kernel=l1_kernel_name(plan)),
             "clocks": clocks.summary(),
             "gathered_bytes_roofline": gathered_bytes_block(sum(bytes_.values()), sec, hbm_gbs,
-                                                    flops / (bf16_tf * 1e12)),
+                                                            flops / (bf16_tf * 1e12)),
             "plan": {k: v for k, v in plan.info.as_dict().items() if k in ("num_ctas", "num_items", "stages",
                                                                             "mma_n", "rows_per_item", "mma_issuers",
                                                                             "cta_pairs", "split_tiles",
